@@ -1,0 +1,241 @@
+"""CPU oracle for the mixed-precision cast-and-scale path (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()``
+and the benchmark's CPU-baseline leg may import this package.  The product
+library never loads it, and it never loads the product library.
+
+The arithmetic lives in plain C (``fp_formats.c``, ``gradscaler.c``,
+``fp8_quant.c``), compiled with ``gcc -O2 -ffp-contract=off``.  This module
+only builds that library and marshals numpy arrays into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SOURCES = ["fp_formats.c", "gradscaler.c", "fp8_quant.c"]
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F16, BF16, F32 = 0, 1, 2
+E4M3, E5M2 = 0, 1
+
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-Wall", "-Wextra"]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its sources (gcc, a second or two)."""
+    srcs = [os.path.join(_HERE, s) for s in _SOURCES]
+    hdr = os.path.join(_HERE, "oracle.h")
+    newest = max(os.path.getmtime(p) for p in srcs + [hdr])
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= newest:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *_CFLAGS, "-o", tmp, *srcs, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        i64, i32, f32p = ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_float)
+        vp = ctypes.c_void_p
+        sig = {
+            "orc_f16_decode": (ctypes.c_double, [ctypes.c_uint16]),
+            "orc_bf16_decode": (ctypes.c_double, [ctypes.c_uint16]),
+            "orc_fp8_decode": (ctypes.c_double, [ctypes.c_uint8, ctypes.c_int]),
+            "orc_f16_encode": (ctypes.c_uint16, [ctypes.c_float]),
+            "orc_bf16_encode": (ctypes.c_uint16, [ctypes.c_float]),
+            "orc_fp8_encode": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_int]),
+            "orc_fp8_max": (ctypes.c_double, [ctypes.c_int]),
+            "orc_decode_array": (None, [vp, ctypes.c_int, i64, vp]),
+            "orc_encode_array": (None, [vp, i64, ctypes.c_int, vp]),
+            "orc_fp8_encode_array": (None, [vp, i64, ctypes.c_int, vp]),
+            "orc_fp8_decode_array": (None, [vp, i64, ctypes.c_int, vp]),
+            "orc_unscale_check": (i32, [vp, i64, ctypes.c_float, vp]),
+            "orc_scaler_update": (None, [f32p, ctypes.POINTER(i32), ctypes.POINTER(i64), i32,
+                                         ctypes.c_float, ctypes.c_float, i32]),
+            "orc_quant_block": (None, [vp, ctypes.c_int, i64, i64, i64, i64, ctypes.c_int, vp, vp]),
+            "orc_quant_tensor": (None, [vp, ctypes.c_int, i64, ctypes.c_int, vp, vp]),
+            "orc_dequant": (None, [vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp]),
+            "orc_amax": (ctypes.c_float, [vp, ctypes.c_int, i64]),
+            "orc_scale_from_amax": (ctypes.c_float, [ctypes.c_float, ctypes.c_int]),
+            "orc_quant_one": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_float, ctypes.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _dtype_code(a: np.ndarray, dtype: int | None) -> int:
+    if dtype is not None:
+        return dtype
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.float16:
+        return F16
+    raise TypeError("uint16 arrays need an explicit dtype (F16 or BF16)")
+
+
+# ---- scalar format functions ----------------------------------------------
+
+def f16_decode(h: int) -> float:
+    return _load().orc_f16_decode(h)
+
+
+def bf16_decode(b: int) -> float:
+    return _load().orc_bf16_decode(b)
+
+
+def fp8_decode(c: int, fmt: int) -> float:
+    return _load().orc_fp8_decode(c, fmt)
+
+
+def f16_encode(x: float) -> int:
+    return _load().orc_f16_encode(x)
+
+
+def bf16_encode(x: float) -> int:
+    return _load().orc_bf16_encode(x)
+
+
+def fp8_encode(x: float, fmt: int) -> int:
+    return _load().orc_fp8_encode(x, fmt)
+
+
+def fp8_max(fmt: int) -> float:
+    return _load().orc_fp8_max(fmt)
+
+
+# ---- array format functions -----------------------------------------------
+
+def decode_array(bits: np.ndarray, dtype: int) -> np.ndarray:
+    bits = np.ascontiguousarray(bits)
+    out = np.empty(bits.shape, np.float32)
+    _load().orc_decode_array(_ptr(bits), dtype, bits.size, _ptr(out))
+    return out
+
+
+def encode_array(x: np.ndarray, dtype: int) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _load().orc_encode_array(_ptr(x), x.size, dtype, _ptr(out))
+    return out
+
+
+def fp8_encode_array(x: np.ndarray, fmt: int) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().orc_fp8_encode_array(_ptr(x), x.size, fmt, _ptr(out))
+    return out
+
+
+def fp8_decode_array(c: np.ndarray, fmt: int) -> np.ndarray:
+    c = np.ascontiguousarray(c, dtype=np.uint8)
+    out = np.empty(c.shape, np.float32)
+    _load().orc_fp8_decode_array(_ptr(c), c.size, fmt, _ptr(out))
+    return out
+
+
+# ---- dynamic loss scaling -------------------------------------------------
+
+def unscale_check(g_bits: np.ndarray, scale: float) -> tuple[np.ndarray, int]:
+    """fp16 bit patterns -> (fp32 unscaled values, found_inf 0/1)."""
+    g_bits = np.ascontiguousarray(g_bits, dtype=np.uint16)
+    out = np.empty(g_bits.shape, np.float32)
+    found = _load().orc_unscale_check(_ptr(g_bits), g_bits.size, scale, _ptr(out))
+    return out, int(found)
+
+
+class ScalerState:
+    """The scaler's whole state: S (fp32), growth tracker, skipped-step count."""
+
+    def __init__(self, scale: float = 65536.0, growth_tracker: int = 0, skipped: int = 0):
+        self.scale = ctypes.c_float(scale)
+        self.growth_tracker = ctypes.c_int32(growth_tracker)
+        self.skipped = ctypes.c_int64(skipped)
+
+    def update(self, found: int, growth_factor: float = 2.0, backoff_factor: float = 0.5,
+               growth_interval: int = 2000) -> None:
+        _load().orc_scaler_update(ctypes.byref(self.scale), ctypes.byref(self.growth_tracker),
+                                  ctypes.byref(self.skipped), int(found), growth_factor,
+                                  backoff_factor, growth_interval)
+
+    def step(self, grads: list[np.ndarray], growth_factor: float = 2.0,
+             backoff_factor: float = 0.5, growth_interval: int = 2000):
+        """Unscale every tensor with the current S, OR the flags, update S."""
+        outs, found = [], 0
+        for g in grads:
+            o, f = unscale_check(g, self.scale.value)
+            outs.append(o)
+            found |= f
+        self.update(found, growth_factor, backoff_factor, growth_interval)
+        return outs, found
+
+
+# ---- FP8 quantisation -----------------------------------------------------
+
+def quant_block(x: np.ndarray, br: int, bc: int, fmt: int, dtype: int | None = None):
+    """Row-major [R, C] input -> (uint8 codes [R, C], fp32 scales [R/br, C/bc])."""
+    x = np.ascontiguousarray(x)
+    code = _dtype_code(x, dtype)
+    R, C = x.shape
+    assert R % br == 0 and C % bc == 0
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R // br, C // bc), np.float32)
+    _load().orc_quant_block(_ptr(x), code, R, C, br, bc, fmt, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_tensor(x: np.ndarray, fmt: int, dtype: int | None = None):
+    """Any-shape input -> (uint8 codes, fp32 scale as a 1-element array)."""
+    x = np.ascontiguousarray(x)
+    code = _dtype_code(x, dtype)
+    q = np.empty(x.shape, np.uint8)
+    s = np.empty((1,), np.float32)
+    _load().orc_quant_tensor(_ptr(x), code, x.size, fmt, _ptr(q), _ptr(s))
+    return q, s
+
+
+def dequant(q: np.ndarray, scales: np.ndarray, br: int, bc: int, fmt: int,
+            out_dtype: int = F32) -> np.ndarray:
+    """codes [R, C] + scales -> fp32 (or bf16 bit patterns when out_dtype=BF16)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    R, C = q.shape
+    y = np.empty((R, C), np.float32 if out_dtype == F32 else np.uint16)
+    _load().orc_dequant(_ptr(q), _ptr(scales), R, C, br, bc, fmt, out_dtype, _ptr(y))
+    return y
+
+
+def amax(x: np.ndarray, dtype: int | None = None) -> float:
+    x = np.ascontiguousarray(x)
+    return _load().orc_amax(_ptr(x), _dtype_code(x, dtype), x.size)
+
+
+def scale_from_amax(a: float, fmt: int) -> float:
+    return _load().orc_scale_from_amax(a, fmt)
+
+
+def quant_one(x: float, s: float, fmt: int) -> int:
+    return _load().orc_quant_one(x, s, fmt)
