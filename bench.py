@@ -1,0 +1,539 @@
+#!/usr/bin/env python
+"""Benchmark of the mixed-precision cast-and-scale path on GB300.
+
+One step = one pass of every row of the hot path over one batch of
+synthetic inputs resident in HBM:
+  * gs_unscale_check_update over the Llama-3-8B-shaped FP16 gradient list
+    (290 tensors, 8,030,257,152 elements; a NaN planted on every 4th step),
+  * fp8_quant_block E4M3 1x128 of a bf16 [16384, 8192] activation with
+    outlier channels, then fp8_dequant of it back to bf16,
+  * fp8_quant_block E4M3 128x128 of a bf16 8192x28672 weight,
+  * fp8_quant_tensor E5M2 of a bf16 8192x28672 gradient.
+value = algorithmic HBM bytes of the step / device time (GB/s).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--sweep] [--no-e2e]
+Under torchrun (N > 1) every rank runs its own replica of the step on its
+own GPU (no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "HBM GB/s (and % of GB300 peak) for grad unscale/inf-check and FP8 block quantise"
+UNIT = "GB/s"
+WORKLOAD = ("Llama-3-8B fp16 grad list unscale+check+update (290 tensors, 8.03e9 elems) + "
+            "E4M3 1x128 quant/dequant of bf16 [16384,8192] activations + E4M3 128x128 quant of "
+            "bf16 8192x28672 weights + E5M2 per-tensor quant of a bf16 8192x28672 gradient")
+FALLBACK_HBM_GBS = 6800.0
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "unscale_check_update": ["unscale_check.cu", "gs_device.cuh", "gs_internal.h"],
+    "quant_1x128": ["fp8_quant.cu", "gs_device.cuh"],
+    "dequant_1x128_bf16": ["fp8_dequant.cu", "gs_device.cuh"],
+    "quant_128x128_tma": ["fp8_quant_tma.cu", "gs_device.cuh"],
+    "quant_tensor_e5m2": ["fp8_quant.cu", "gs_device.cuh"],
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--sweep", action="store_true", help="bandwidth sweep 1 MiB..8 GiB (config 5)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args(argv)
+
+
+# ---- multi-process plumbing ---------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, init_method="env://")
+    return dist if world > 1 else None
+
+
+def aggregate(elapsed_s: float, units: float, dist=None, device=None) -> tuple[float, float]:
+    """Max elapsed time over ranks and total units over ranks."""
+    if dist is None:
+        return elapsed_s, units
+    import torch
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def throughput(total_bytes: float, elapsed_s: float) -> float:
+    return total_bytes / elapsed_s / 1e9
+
+
+# ---- peaks, traffic, clocks --------------------------------------------------------
+
+def hbm_peak() -> tuple[float, str]:
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def sources_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "mixed_precision_numerics_gradscaler_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel's sources changed since those counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[kernel]
+        return rec["dram_bytes_per_launch"] if rec["sources_sha"] == sources_sha(kernel) else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r[2] > 300.0] or rows   # samples taken under load
+        reasons = sorted({self.NAMES[i] for r in busy for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(busy), "power_w_max": max(r[2] for r in rows)}
+
+
+# ---- the step -------------------------------------------------------------------
+
+class Workload:
+    """Every buffer of one step, resident on the current GPU."""
+
+    def __init__(self, gs, torch, small: bool = False):
+        import datagen as dg
+        from datagen import workloads as wl
+        self.gs, self.torch, self.dg = gs, torch, dg
+        dev = torch.device("cuda", torch.cuda.current_device())
+        st = torch.cuda.current_stream().cuda_stream
+        self.cfg2 = wl.cfg2_grads()
+        f16, f32, bf16, u8 = torch.float16, torch.float32, torch.bfloat16, torch.uint8
+        self.grads = [torch.empty(n, dtype=f16, device=dev) for n in self.cfg2.numels]
+        self.outs = [torch.empty(n, dtype=f32, device=dev) for n in self.cfg2.numels]
+        for t, (g, n) in enumerate(zip(self.grads, self.cfg2.numels)):
+            dg.fill_device(self.cfg2.spec(t, 0), 0, n, g.data_ptr(), st)
+        self.tl = gs.gs_tensor_list_create(self.grads, self.outs)
+        self.scale = torch.tensor([self.cfg2.init_scale], dtype=f32, device=dev)
+        self.tracker = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.found = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.skipped = torch.zeros(1, dtype=torch.int64, device=dev)
+        a, w, g = wl.cfg3_act(), wl.cfg4_weight(), wl.cfg4_grad()
+        self.x3 = torch.empty(a.rows, a.cols, dtype=bf16, device=dev)
+        dg.fill_device(a.spec, 0, a.numel, self.x3.data_ptr(), st)
+        self.q3 = torch.empty(a.rows, a.cols, dtype=u8, device=dev)
+        self.s3 = torch.empty(a.rows, a.cols // 128, dtype=f32, device=dev)
+        self.y3 = torch.empty(a.rows, a.cols, dtype=bf16, device=dev)
+        self.x4 = torch.empty(w.rows, w.cols, dtype=bf16, device=dev)
+        dg.fill_device(w.spec, 0, w.numel, self.x4.data_ptr(), st)
+        self.q4 = torch.empty(w.rows, w.cols, dtype=u8, device=dev)
+        self.s4 = torch.empty(w.rows // 128, w.cols // 128, dtype=f32, device=dev)
+        self.x5 = torch.empty(g.numel, dtype=bf16, device=dev)
+        dg.fill_device(g.spec, 0, g.numel, self.x5.data_ptr(), st)
+        self.q5 = torch.empty(g.numel, dtype=u8, device=dev)
+        self.s5 = torch.empty(1, dtype=f32, device=dev)
+        self.ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=dev)
+        # NaN planted on every 4th step at a seeded (tensor, index)
+        t, i = self.cfg2.plant(4)
+        self.plant_ptr = self.grads[t].data_ptr() + 2 * i
+        self.plant_orig = int(dg.fill_host_idx(self.cfg2.spec(t, 0), __import__("numpy").array([i]))[0])
+        n2, n3, n4, n5 = self.cfg2.total, a.numel, w.numel, g.numel
+        self.bytes = {
+            "unscale_check_update": 6 * n2,
+            "quant_1x128": 3 * n3 + 4 * (n3 // 128),
+            "dequant_1x128_bf16": 3 * n3 + 4 * (n3 // 128),
+            "quant_128x128_tma": 3 * n4 + 4 * (n4 // 16384),
+            "quant_tensor_e5m2": 5 * n5 + 4,
+        }
+        self.launches = {"unscale_check_update": 1, "quant_1x128": 1, "dequant_1x128_bf16": 1,
+                         "quant_128x128_tma": 1, "quant_tensor_e5m2": 2}
+        torch.cuda.synchronize()
+
+    @property
+    def bytes_per_step(self) -> int:
+        return sum(self.bytes.values())
+
+    @property
+    def launches_per_step(self) -> int:
+        return sum(self.launches.values())
+
+    def step(self, k: int, events=None):
+        gs, torch = self.gs, self.torch
+        st = torch.cuda.current_stream().cuda_stream
+        nan_step = (k % 4) == 3
+
+        def mark(name, fn):
+            if events is None:
+                fn()
+                return
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            events.append((name, e0, e1))
+
+        if nan_step:
+            self.dg.plant_device(self.plant_ptr, 0x7E00, st)
+        mark("unscale_check_update", lambda: gs.gs_unscale_check_update(
+            self.tl, self.scale, self.tracker, self.found, self.skipped, 2.0, 0.5, 2000))
+        if nan_step:
+            self.dg.plant_device(self.plant_ptr, self.plant_orig, st)
+        mark("quant_1x128", lambda: gs.fp8_quant_block(self.x3, 1, 128, "e4m3", self.q3, self.s3))
+        mark("dequant_1x128_bf16", lambda: gs.fp8_dequant(self.q3, self.s3, 1, 128, "e4m3", self.y3))
+        mark("quant_128x128_tma", lambda: gs.fp8_quant_block(self.x4, 128, 128, "e4m3", self.q4, self.s4))
+        mark("quant_tensor_e5m2", lambda: gs.fp8_quant_tensor(self.x5, "e5m2", self.q5, self.s5, self.ws))
+
+    # -- end to end: host (pinned) buffers, copies inside the timed region ----
+    def e2e_setup(self):
+        torch = self.torch
+        pin = dict(pin_memory=True)
+        self.h_in = [torch.empty(g.shape, dtype=g.dtype, **pin) for g in
+                     self.grads + [self.x3, self.x4, self.x5]]
+        self.d_in = self.grads + [self.x3, self.x4, self.x5]
+        for h, d in zip(self.h_in, self.d_in):
+            h.copy_(d)
+        self.d_out = self.outs + [self.q3, self.s3, self.y3, self.q4, self.s4, self.q5, self.s5,
+                                  self.scale, self.tracker, self.found]
+        self.h_out = [torch.empty(d.shape, dtype=d.dtype, **pin) for d in self.d_out]
+        torch.cuda.synchronize()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.h_in)
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.d_out)
+
+    def e2e_step(self, k: int):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        self.step(k)
+        for h, d in zip(self.h_out, self.d_out):
+            h.copy_(d, non_blocking=True)
+
+
+# ---- CPU oracle baseline ---------------------------------------------------------
+
+class OracleSample:
+    """A bounded sample of the same step, run by the CPU oracle: the first
+    elements of the gradient list, whole rows of the activation, whole
+    128-row block-rows of the weight, a slice of the gradient, in roughly
+    the step's byte proportions (fraction `frac` of the full step)."""
+
+    def __init__(self, frac: float = 1.0 / 1000):
+        import numpy as np
+        import datagen as dg
+        from datagen import workloads as wl
+        self.np = np
+        cfg2 = wl.cfg2_grads()
+        self.n_u = max(8, int(cfg2.total * frac))
+        self.g_bits = dg.fill_host(cfg2.spec(0, 0), 0, self.n_u)
+        a = wl.cfg3_act()
+        self.rows3 = max(1, int(a.rows * frac))
+        self.x3 = dg.fill_host(a.spec, 0, self.rows3 * a.cols).reshape(self.rows3, a.cols)
+        w = wl.cfg4_weight()
+        self.blocks4 = max(1, int(round(w.numel * frac / 16384)))
+        cols4 = 128 * self.blocks4
+        self.x4 = np.stack([dg.fill_host(w.spec, r * w.cols, cols4) for r in range(128)])
+        g = wl.cfg4_grad()
+        self.n5 = max(1, int(g.numel * frac))
+        self.x5 = dg.fill_host(g.spec, 0, self.n5)
+        n3, n4 = self.x3.size, self.x4.size
+        self.bytes = (6 * self.n_u + 2 * (3 * n3 + 4 * (n3 // 128)) + 3 * n4 + 4 * (n4 // 16384)
+                      + 5 * self.n5)
+        self.desc = (f"oracle on {self.n_u} grad elems + {self.rows3}x{a.cols} act (1x128 quant + "
+                     f"bf16 dequant) + 128x{cols4} weight (128x128) + {self.n5} grad elems "
+                     f"(E5M2 per-tensor): {frac:.4g} of one step")
+
+    def run(self):
+        import oracle as orc
+        orc.unscale_check(self.g_bits, 65536.0)
+        q, s = orc.quant_block(self.x3, 1, 128, orc.E4M3, dtype=orc.BF16)
+        orc.dequant(q, s, 1, 128, orc.E4M3, out_dtype=orc.BF16)
+        orc.quant_block(self.x4, 128, 128, orc.E4M3, dtype=orc.BF16)
+        orc.quant_tensor(self.x5, orc.E5M2, dtype=orc.BF16)
+
+
+def cpu_baseline(seconds: float) -> dict:
+    sample = OracleSample()
+    sample.run()  # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        sample.run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": throughput(sample.bytes * reps, el), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{sample.desc}; {reps} repetitions in {el:.1f} s, single thread"}
+
+
+# ---- arms -----------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    sample = OracleSample()
+    for k in range(args.warmup):
+        sample.run()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        sample.run()
+    el = time.perf_counter() - t0
+    value = throughput(sample.bytes * args.steps, el)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": WORKLOAD, "reference": "CPU oracle (plain C, scalar), the "
+                       "pages ship no implementation", "sample_bytes_per_step": sample.bytes},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample.desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def gpu_uuid(torch, dev_index: int) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev_index)
+
+
+def run_ours(args):
+    import torch
+    import mixed_precision_numerics_gradscaler_gb300 as gs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    w = Workload(gs, torch)
+
+    for k in range(args.warmup):
+        w.step(k)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    events = []
+    with ClockSampler(gpu_uuid(torch, local)) as clocks:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record()
+        for k in range(args.steps):
+            w.step(args.warmup + k, events)
+        t_end.record()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    elapsed = t_start.elapsed_time(t_end) / 1000.0
+    max_el, total_bytes = aggregate(elapsed, float(w.bytes_per_step * args.steps), dist, dev)
+    value = throughput(total_bytes, max_el)
+
+    per = {}
+    for name, e0, e1 in events:
+        per.setdefault(name, []).append(e0.elapsed_time(e1))
+    peak, peak_src = hbm_peak()
+    kernels = {}
+    for name, ts in per.items():
+        ms = sum(ts) / len(ts)
+        gbs = w.bytes[name] / (ms / 1000.0) / 1e9
+        kernels[name] = {"avg_ms": round(ms, 4), "bytes": w.bytes[name], "gbs": round(gbs, 1),
+                         "frac": round(gbs / peak, 4), "launches_per_step": w.launches[name]}
+    dom = max(kernels, key=lambda n: kernels[n]["avg_ms"])
+    roofline = {"bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak, "unit": UNIT,
+                "frac": kernels[dom]["frac"], "traffic": measured_traffic(dom), "kernel": dom,
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})",
+                "frac_of_8tbs_nominal": round(kernels[dom]["gbs"] / 8000.0, 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        w.e2e_setup()
+        for k in range(1):
+            w.e2e_step(k)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for k in range(args.e2e_steps):
+            w.e2e_step(k)
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        if dist:
+            dist.barrier()
+        max_e2e, tot = aggregate(el, float(w.bytes_per_step * args.e2e_steps), dist, dev)
+        e2e = {"value": throughput(tot, max_e2e), "unit": UNIT,
+               "h2d_bytes_per_step": w.h2d_bytes, "d2h_bytes_per_step": w.d2h_bytes,
+               "steps": args.e2e_steps, "ms_per_step": 1000 * max_e2e / args.e2e_steps}
+
+    cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1) else None
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1000 * max_el / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic (seeded counter-based generator, inputs resident in HBM)",
+                "config": {"workload": WORKLOAD, "bytes_per_step": w.bytes_per_step,
+                           "l2": "no flush: every input (16 GB, 268 MB, 470 MB, 470 MB) is larger "
+                                 "than the 129 MB L2", "parallelism": f"replicas x{world}"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": w.launches_per_step * args.steps,
+                "clocks": clocks.summary(), "kernels": kernels,
+                "state_after": {"scale": float(w.scale.item()), "skipped": int(w.skipped.item())}}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(args):
+    """Config 5: GB/s of unscale (one flat fp16 tensor) and of 1x128 E4M3
+    quantisation (bf16 [bytes/16384, 8192]) for inputs of 1 MiB .. 8 GiB."""
+    import torch
+    import datagen as dg
+    from datagen import workloads as wl
+    import mixed_precision_numerics_gradscaler_gb300 as gs
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream().cuda_stream
+    peak, src = hbm_peak()
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    points = []
+    for nbytes in wl.cfg5_sizes():
+        n = nbytes // 2
+        g = torch.empty(n, dtype=torch.float16, device="cuda")
+        lo, hi = wl.binades(-10, -1, 16)
+        dg.fill_device(dg.logu_f16(wl.seed_of(5), 0, lo, hi), 0, n, g.data_ptr(), st)
+        o = torch.empty(n, dtype=torch.float32, device="cuda")
+        tl = gs.gs_tensor_list_create([g], [o])
+        sc = torch.tensor([65536.0], device="cuda")
+        tr = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fi = torch.zeros(1, dtype=torch.int32, device="cuda")
+        x = g.view(torch.bfloat16).view(-1, 8192) if n % 8192 == 0 else None
+        res = {"input_bytes": nbytes, "cache_resident": nbytes < 2 * 129 * 2 ** 20}
+        for name, fn, b in [
+            ("unscale", lambda: gs.gs_unscale_check_update(tl, sc, tr, fi, None, 2.0, 0.5, 2000), 6 * n)]:
+            ts = []
+            for r in range(max(args.warmup, 3) + 10):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                if r >= max(args.warmup, 3):
+                    ts.append(e0.elapsed_time(e1))
+            ms = statistics.median(ts)
+            res[name] = {"ms": ms, "gbs": b / ms / 1e6, "frac": b / ms / 1e6 / peak}
+        if x is not None:
+            q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+            s = torch.empty(x.shape[0], 64, dtype=torch.float32, device="cuda")
+            nb = 3 * n + 4 * (n // 128)
+            ts = []
+            for r in range(max(args.warmup, 3) + 10):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)
+                e1.record()
+                torch.cuda.synchronize()
+                if r >= max(args.warmup, 3):
+                    ts.append(e0.elapsed_time(e1))
+            ms = statistics.median(ts)
+            res["quant_1x128"] = {"ms": ms, "gbs": nb / ms / 1e6, "frac": nb / ms / 1e6 / peak}
+            del q, s
+        points.append(res)
+        tl.close()
+        del g, o
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": METRIC, "unit": UNIT, "peak": peak, "peak_source": src,
+                      "l2": "512 MiB buffer zeroed before every timed launch", "sweep": points}))
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

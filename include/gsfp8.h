@@ -1,0 +1,192 @@
+/*
+ * gsfp8.h -- C ABI of the GB300 (sm_103a) mixed-precision cast-and-scale
+ * library: dynamic loss scaling of FP16 gradient lists and FP8
+ * quantisation with fine-grained (1x128 / 128x128 / per-tensor) scaling.
+ *
+ * Sources of the definitions (web pages, cited by title and section):
+ *   [P1] "Loss scaling, FP8, and the failure that never crashes"
+ *   [P3] "Numerical Precision, Mixed Precision, and Loss Scaling"
+ *   [P4] "Why FP8 training is stable"
+ *   [P5] "Mixed precision and FP8 training"
+ *
+ * Conventions shared by every entry point:
+ *   - Return value: a gs_status code.  Argument errors are found on the
+ *     host before anything is launched; nothing is enqueued when a call
+ *     returns anything but GS_OK.  GS_ERR_CUDA means a CUDA call made by the
+ *     library failed (see gs_last_cuda_error).  Nothing throws or aborts.
+ *   - Streams: `stream` is a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream.  Every compute call is asynchronous on that
+ *     stream and never synchronises the host.
+ *   - Memory: every data pointer is device memory of the current device
+ *     (or managed / mapped host memory the device can reach); pointers the
+ *     device cannot reach are rejected with GS_ERR_ARG.  The caller owns all
+ *     data buffers.  The library allocates only inside
+ *     gs_tensor_list_create; no compute call allocates.
+ *   - Layout: row-major and contiguous; element [r, c] of an R x C array is
+ *     at offset r * C + c.  Outputs must not overlap inputs.  Any element-
+ *     aligned address is accepted; 16-byte-aligned buffers take the
+ *     vectorised paths.
+ *   - Device-side waits are bounded: a kernel that gives up on a wait
+ *     records GS_ERR_TIMEOUT in a device status word (gs_device_status)
+ *     and returns; it never traps.
+ */
+#ifndef GSFP8_H
+#define GSFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gs_status {
+  GS_OK = 0,
+  GS_ERR_NULL = 1,    /* a required pointer is NULL                          */
+  GS_ERR_SHAPE = 2,   /* sizes negative, not divisible by the block, too big */
+  GS_ERR_DTYPE = 3,   /* unsupported element type or FP8 format              */
+  GS_ERR_ARG = 4,     /* other invalid argument (pointer not reachable, ...) */
+  GS_ERR_CUDA = 5,    /* a CUDA runtime call failed                          */
+  GS_ERR_TIMEOUT = 6  /* a bounded device-side wait expired                  */
+} gs_status;
+
+typedef enum gs_dtype { GS_F16 = 0, GS_BF16 = 1, GS_F32 = 2 } gs_dtype;
+
+/* OCP FP8 encodings ([P3] paragraph on the FP8 specification; [P4]
+ * "Failure 2"): E4M3 -- bias 7, max 448 (S.1111.110), no infinities, one
+ * NaN pattern; E5M2 -- bias 15, max 57344 (S.11110.11), IEEE-style Inf/NaN.
+ * Casts are round-to-nearest-even and saturating (|v| beyond max and +-Inf
+ * give +-max); every NaN is written as 0x7F. */
+typedef enum gs_fp8 { GS_E4M3 = 0, GS_E5M2 = 1 } gs_fp8;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* gs_status_str(int status);
+
+/* The cudaError_t of the most recent GS_ERR_CUDA on the calling thread. */
+int gs_last_cuda_error(void);
+
+/* Library version string. */
+const char* gs_version(void);
+
+/* ------------------------------------------------------------------------
+ * Dynamic loss scaling ([P1] "Loss scaling, derived from the chain rule you
+ * already have" and its SimpleGradScaler listing; [P3] GradScaler defaults
+ * paragraph and its six-step training step, step 4 "unscale and inspect"
+ * and step 6 "adjust the dynamic loss scale").
+ * --------------------------------------------------------------------- */
+
+/* Opaque description of one gradient list: for each tensor, its scaled
+ * FP16 gradient (input), its FP32 unscaled output and its element count.
+ * The handle owns a device-resident table that cuts the list into
+ * equal-sized chunks, built once so that each step walks the whole list in
+ * a single grid, plus a 16-byte device workspace. */
+typedef struct gs_tensor_list gs_tensor_list;
+
+/* Build a list on the current device.
+ *   grads[i]  -- device pointer to numels[i] FP16 values (scaled gradients)
+ *   outs[i]   -- device pointer to numels[i] FP32 values (written by
+ *                gs_unscale_check_update)
+ *   numels[i] -- >= 0; n_tensors >= 0 (0 gives an empty list)
+ * Allocates device memory and copies the chunk table synchronously (the
+ * only allocating call of this library).  The pointers are captured: the
+ * list stays valid while those buffers live.  On error *out is NULL. */
+int gs_tensor_list_create(const void* const* grads, void* const* outs, const int64_t* numels,
+                          int32_t n_tensors, gs_tensor_list** out);
+
+/* Free a list (NULL is accepted).  Synchronises the device first, so it
+ * must not be called while the list is in use by a capture. */
+int gs_tensor_list_destroy(gs_tensor_list* list);
+
+/* Total element count and chunk count of a list (host values). */
+int gs_tensor_list_info(const gs_tensor_list* list, int64_t* total_elems, int64_t* n_chunks);
+
+/* One GradScaler step over the whole list, in one kernel launch:
+ *   out_i = fp32(g_i) * fp32(1 / S)   for every element of every tensor,
+ *           where S is *scale as it was before this call; written on
+ *           skipped steps too (the caller skips the optimizer);
+ *   found_inf = 1 if any g_i is Inf or NaN (exponent field all ones, tested
+ *           on the scaled FP16 input), else 0;
+ *   then, on the device, after every element has been checked:
+ *     found_inf: S *= backoff_factor, growth_tracker = 0, *skipped += 1;
+ *     otherwise: growth_tracker += 1 and, if growth_tracker >=
+ *                growth_interval, S *= growth_factor, growth_tracker = 0.
+ * scale, growth_tracker, found_inf: device scalars (fp32, int32, int32);
+ * skipped: device int64 or NULL.  The host never reads any of them.
+ * growth_interval >= 1; factors finite and > 0.  (PyTorch-style defaults:
+ * S0 = 65536, growth 2.0, backoff 0.5, interval 2000; a static scale is
+ * growth_factor = backoff_factor = 1.)  Calls that use the same list must
+ * be ordered on one stream (the list's workspace is reused each call). */
+int gs_unscale_check_update(const gs_tensor_list* list, float* scale, int32_t* growth_tracker,
+                            int32_t* found_inf, int64_t* skipped, float growth_factor,
+                            float backoff_factor, int32_t growth_interval, void* stream);
+
+/* Checkpoint support: the scaler's whole state is {S, growth_tracker}.
+ * get: copies the two device scalars to host variables and waits for the
+ *      copy on `stream` (this call synchronises that stream).
+ * set: writes host values into the device scalars, stream-ordered
+ *      (asynchronous; the values are passed by value, no host buffer is
+ *      kept). */
+int gs_scaler_state_get(const float* scale, const int32_t* growth_tracker, float* h_scale,
+                        int32_t* h_growth_tracker, void* stream);
+int gs_scaler_state_set(float* scale, int32_t* growth_tracker, float h_scale,
+                        int32_t h_growth_tracker, void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 quantisation with fine-grained scaling ([P5] "FP8 training", the
+ * fp8_scaling.py listing: per-block amax, clamp at 1e-12, divide by MAX;
+ * quantise x / s with clamp to +-MAX and cast; dequantise by multiplying
+ * by s.  [P1] "FP8 needs a finer-grained fix than a single scale factor"
+ * and [P4] "The seam": 1x128 tiles for activations, 128x128 blocks for
+ * weights.  [P4] "Failure 1": per-tensor current scaling.)
+ *
+ * For each block B:   amax_B = max |x| over B (a NaN in B makes it NaN)
+ *                     s_B    = max(amax_B, 1e-12f) / MAX      (fp32)
+ *                     q      = fp8(clamp(x / s_B, -MAX, MAX)) (fp32 x/s,
+ *                              round to nearest even)
+ * MAX = 448 (E4M3) or 57344 (E5M2).
+ * --------------------------------------------------------------------- */
+
+/* Block-scaled quantisation of a row-major [R, C] tensor.
+ *   x        -- R*C elements of in_dtype (GS_BF16, GS_F16 or GS_F32)
+ *   (block_r, block_c) -- (1, 128): 1x128 tiles along the contiguous
+ *               dimension; or (128, 128): square blocks.  R % block_r == 0
+ *               and C % block_c == 0, else GS_ERR_SHAPE.
+ *   q        -- R*C bytes of FP8 codes (fmt)
+ *   scales   -- fp32 [R / block_r, C / block_c], row-major
+ * R == 0 or C == 0 is a valid no-op. */
+int fp8_quant_block(const void* x, int in_dtype, int64_t R, int64_t C, int32_t block_r,
+                    int32_t block_c, int fmt, uint8_t* q, float* scales, void* stream);
+
+/* Bytes of device workspace fp8_quant_tensor needs (independent of n). */
+size_t gs_ws_bytes(void);
+
+/* Per-tensor (current) scaling of n elements: one scale for the whole
+ * tensor, computed in a first pass over x and used by a second pass, both
+ * on the device (the host never reads amax).
+ *   scale -- device fp32 [1], written;  ws -- device workspace of at least
+ *   gs_ws_bytes() bytes, 4-byte aligned, any contents (fully overwritten).
+ * Calls sharing one ws must be ordered on one stream. */
+int fp8_quant_tensor(const void* x, int in_dtype, int64_t n, int fmt, uint8_t* q, float* scale,
+                     void* ws, void* stream);
+
+/* Dequantise: y = decode(q) * s (fp32 product), stored as fp32 or rounded
+ * to nearest-even bfloat16 (out_dtype GS_F32 or GS_BF16).
+ * Block shapes: (1, 128) and (128, 128) with scales laid out as written by
+ * fp8_quant_block, or (R, C) -- one scale for the whole [R, C] tensor, as
+ * written by fp8_quant_tensor (use R = 1, C = n for a flat tensor). */
+int fp8_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C, int32_t block_r,
+                int32_t block_c, int fmt, int out_dtype, void* y, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ * --------------------------------------------------------------------- */
+
+/* Reads and clears the device status word of the current device
+ * (GS_OK or GS_ERR_TIMEOUT recorded by a kernel that gave up waiting).
+ * Synchronises `stream`. */
+int gs_device_status(int32_t* h_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GSFP8_H */

@@ -1,0 +1,405 @@
+// fp8_quant.cu -- FP8 quantisation with fine-grained scaling ("Mixed
+// precision and FP8 training", section "FP8 training": per-block amax,
+// clamp at 1e-12, divide by MAX; q = cast(clamp(x / s)); "Loss scaling,
+// FP8, and the failure that never crashes", section "FP8 needs a
+// finer-grained fix than a single scale factor": 1x128 tiles for
+// activations, 128x128 blocks for weights; "Why FP8 training is stable",
+// "Failure 1": per-tensor current scaling).
+//
+// Kernels:
+//   quant_1x128_v16  -- BF16/FP16 input, 16-byte aligned: one 16-lane group
+//                       per 1x128 tile (8 elements per lane), amax by a
+//                       4-step shuffle on magnitude bit patterns.
+//   quant_1x128_v32  -- FP32 input, aligned: one warp per tile.
+//   quant_1x128_any  -- any dtype / alignment: one warp per tile, scalar.
+//   quant_128x128_any-- any dtype / alignment: one CTA per block, two
+//                       passes over the block (the second hits L2).  The
+//                       TMA-staged 128x128 kernel lives in fp8_quant_tma.cu.
+//   amax_partials + quant_tensor -- the two passes of per-tensor scaling.
+// All paths are HBM-bound: 1x128 moves 2 + 1 + 4/128 bytes per BF16 element.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+constexpr int kQuantThreads = 256;
+constexpr int kQuantUnroll = 4;
+
+// ---- generic element access (fallback paths) -------------------------------
+template <int DT>
+__device__ __forceinline__ uint32_t mag_bits(const void* x, int64_t i) {
+  if constexpr (DT == GS_F32) return reinterpret_cast<const uint32_t*>(x)[i] & 0x7FFFFFFFu;
+  else return reinterpret_cast<const uint16_t*>(x)[i] & 0x7FFFu;
+}
+template <int DT>
+__device__ __forceinline__ float mag_to_float(uint32_t m) {
+  if constexpr (DT == GS_F32) return __uint_as_float(m);
+  else if constexpr (DT == GS_BF16) return __uint_as_float(m << 16);
+  else return __half2float(__ushort_as_half((unsigned short)m));
+}
+template <int DT>
+__device__ __forceinline__ float load_f(const void* x, int64_t i) {
+  if constexpr (DT == GS_F32) return reinterpret_cast<const float*>(x)[i];
+  else if constexpr (DT == GS_BF16)
+    return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[i] << 16);
+  else return __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(x)[i]));
+}
+
+template <int FMT>
+__device__ __forceinline__ uint8_t quant_one(float v, float s, float r, bool fin) {
+  return (uint8_t)(quant_pair<FMT>(0.0f, v, s, r, fin) & 0xFFu);
+}
+
+__device__ __forceinline__ uint32_t warp_max(uint32_t m) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  return m;
+}
+
+// ---- 1x128, 16-bit input, vectorised ---------------------------------------
+template <typename Tag, int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_1x128_v16(const uint4* __restrict__ x, int64_t n_tiles, uint2* __restrict__ q,
+                    float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t n_pairs = (n_tiles + 1) >> 1;
+  // The loop bound is uniform across the warp, so every lane reaches the
+  // shuffles; lanes whose tile is past the end load nothing, store nothing.
+  for (int64_t p0 = warp; p0 < n_pairs; p0 += n_warps * kQuantUnroll) {
+    uint4 v[kQuantUnroll];
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t t = 2 * (p0 + u * n_warps) + half;
+      v[u] = (t < n_tiles) ? ld_stream(x + t * 16 + l16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t t = 2 * (p0 + u * n_warps) + half;
+      const uint32_t mm = 0x7FFF7FFFu;
+      uint32_t m = __vmaxu2(__vmaxu2(v[u].x & mm, v[u].y & mm), __vmaxu2(v[u].z & mm, v[u].w & mm));
+      m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
+      const bool fin = isfinite(s);
+      const float r = __frcp_rn(s);
+      uint2 o;
+      o.x = quant_pair<FMT>(hi16<Tag>(v[u].x), lo16<Tag>(v[u].x), s, r, fin) |
+            (quant_pair<FMT>(hi16<Tag>(v[u].y), lo16<Tag>(v[u].y), s, r, fin) << 16);
+      o.y = quant_pair<FMT>(hi16<Tag>(v[u].z), lo16<Tag>(v[u].z), s, r, fin) |
+            (quant_pair<FMT>(hi16<Tag>(v[u].w), lo16<Tag>(v[u].w), s, r, fin) << 16);
+      if (t < n_tiles) {
+        st_stream(q + t * 16 + l16, o);
+        if (l16 == 0) scales[t] = s;
+      }
+    }
+  }
+}
+
+// ---- 1x128, FP32 input, vectorised: one warp per tile ------------------------
+template <int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_1x128_v32(const uint4* __restrict__ x, int64_t n_tiles, uint32_t* __restrict__ q,
+                    float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = warp; t < n_tiles; t += n_warps) {
+    const uint4 v = ld_stream(x + t * 32 + lane);
+    const uint32_t mm = 0x7FFFFFFFu;
+    uint32_t m = max(max(v.x & mm, v.y & mm), max(v.z & mm, v.w & mm));
+    m = warp_max(m);
+    const float s = block_scale<FMT>(__uint_as_float(m));
+    const bool fin = isfinite(s);
+    const float r = __frcp_rn(s);
+    const uint32_t c = quant_pair<FMT>(__uint_as_float(v.y), __uint_as_float(v.x), s, r, fin) |
+                       (quant_pair<FMT>(__uint_as_float(v.w), __uint_as_float(v.z), s, r, fin) << 16);
+    q[t * 32 + lane] = c;
+    if (lane == 0) scales[t] = s;
+  }
+}
+
+// ---- 1x128, any dtype and alignment ------------------------------------------
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_1x128_any(const void* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ q,
+                    float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = warp; t < n_tiles; t += n_warps) {
+    const int64_t base = t * 128;
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = max(m, mag_bits<DT>(x, base + lane + 32 * k));
+    m = warp_max(m);
+    const float s = block_scale<FMT>(mag_to_float<DT>(m));
+    const bool fin = isfinite(s);
+    const float r = __frcp_rn(s);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = base + lane + 32 * k;
+      q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
+    }
+    if (lane == 0) scales[t] = s;
+  }
+}
+
+// ---- 128x128, any dtype and alignment: one CTA per block --------------------
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_128x128_any(const void* __restrict__ x, int64_t R, int64_t C, uint8_t* __restrict__ q,
+                      float* __restrict__ scales) {
+  __shared__ uint32_t red[kQuantThreads / 32];
+  __shared__ float s_sh;
+  const int64_t nbc = C / 128, n_blocks = (R / 128) * nbc;
+  for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
+    const int64_t r0 = (b / nbc) * 128, c0 = (b % nbc) * 128;
+    uint32_t m = 0;
+    for (int k = threadIdx.x; k < 128 * 128; k += blockDim.x)
+      m = max(m, mag_bits<DT>(x, (r0 + (k >> 7)) * C + c0 + (k & 127)));
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t mm = 0;
+      for (int w = 0; w < kQuantThreads / 32; ++w) mm = max(mm, red[w]);
+      const float s = block_scale<FMT>(mag_to_float<DT>(mm));
+      s_sh = s;
+      scales[b] = s;
+    }
+    __syncthreads();
+    const float s = s_sh;
+    const bool fin = isfinite(s);
+    const float r = __frcp_rn(s);
+    for (int k = threadIdx.x; k < 128 * 128; k += blockDim.x) {
+      const int64_t i = (r0 + (k >> 7)) * C + c0 + (k & 127);
+      q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
+    }
+    __syncthreads();  // red / s_sh are reused by the next block
+  }
+}
+
+// ---- per-tensor: pass 1, per-CTA amax partials --------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kQuantThreads)
+    amax_partials(const void* __restrict__ x, int64_t n, uint32_t* __restrict__ partials) {
+  __shared__ uint32_t red[kQuantThreads / 32];
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  uint32_t m = 0;
+  if constexpr (DT != GS_F32) {
+    // 16-byte vectors once the pointer is aligned; scalar head and tail.
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(x);
+    int64_t head = (int64_t)(((16u - ((uint32_t)(uintptr_t)xs & 15u)) & 15u) >> 1);
+    if (head > n) head = n;
+    for (int64_t i = tid; i < head; i += nthreads) m = max(m, (uint32_t)(xs[i] & 0x7FFFu));
+    const int64_t nv = (n - head) >> 3;
+    const uint4* x8 = reinterpret_cast<const uint4*>(xs + head);
+    uint32_t m2 = 0;
+    const uint32_t mm = 0x7FFF7FFFu;
+    int64_t v = tid;
+    for (; v + 3 * nthreads < nv; v += 4 * nthreads) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = ld_stream(x8 + v + u * nthreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a[u].x & mm, a[u].y & mm),
+                                   __vmaxu2(a[u].z & mm, a[u].w & mm)));
+    }
+    for (; v < nv; v += nthreads) {
+      const uint4 a = ld_stream(x8 + v);
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & mm, a.y & mm), __vmaxu2(a.z & mm, a.w & mm)));
+    }
+    m = max(m, max(m2 & 0xFFFFu, m2 >> 16));
+    for (int64_t i = head + nv * 8 + tid; i < n; i += nthreads) m = max(m, (uint32_t)(xs[i] & 0x7FFFu));
+  } else {
+    for (int64_t i = tid; i < n; i += nthreads) m = max(m, mag_bits<DT>(x, i));
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t mm = 0;
+    for (int w = 0; w < kQuantThreads / 32; ++w) mm = max(mm, red[w]);
+    partials[blockIdx.x] = mm;
+  }
+}
+
+// ---- per-tensor: pass 2, reduce the partials, quantise ------------------------
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_tensor_pass2(const void* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
+                       float* __restrict__ scale_out, const uint32_t* __restrict__ partials,
+                       int n_partials) {
+  __shared__ uint32_t red[kQuantThreads / 32];
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < n_partials; i += blockDim.x) m = max(m, partials[i]);
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0;
+#pragma unroll
+  for (int w = 0; w < kQuantThreads / 32; ++w) m = max(m, red[w]);
+  const float s = block_scale<FMT>(mag_to_float<DT>(m));
+  const bool fin = isfinite(s);
+  const float r = __frcp_rn(s);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  if constexpr (DT != GS_F32) {
+    using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(x);
+    // vector body needs x 16-byte and q 8-byte aligned at the same element
+    int64_t head = (int64_t)(((16u - ((uint32_t)(uintptr_t)xs & 15u)) & 15u) >> 1);
+    if (head > n) head = n;
+    if ((((uintptr_t)(q + head)) & 7u) != 0) head = n;
+    for (int64_t i = tid; i < head; i += nthreads) q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
+    const int64_t nv = (n - head) >> 3;
+    const uint4* x8 = reinterpret_cast<const uint4*>(xs + head);
+    uint2* q8 = reinterpret_cast<uint2*>(q + head);
+    int64_t v = tid;
+    for (; v + 3 * nthreads < nv; v += 4 * nthreads) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = ld_stream(x8 + v + u * nthreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint2 o;
+        o.x = quant_pair<FMT>(hi16<Tag>(a[u].x), lo16<Tag>(a[u].x), s, r, fin) |
+              (quant_pair<FMT>(hi16<Tag>(a[u].y), lo16<Tag>(a[u].y), s, r, fin) << 16);
+        o.y = quant_pair<FMT>(hi16<Tag>(a[u].z), lo16<Tag>(a[u].z), s, r, fin) |
+              (quant_pair<FMT>(hi16<Tag>(a[u].w), lo16<Tag>(a[u].w), s, r, fin) << 16);
+        st_stream(q8 + v + u * nthreads, o);
+      }
+    }
+    for (; v < nv; v += nthreads) {
+      const uint4 a = ld_stream(x8 + v);
+      uint2 o;
+      o.x = quant_pair<FMT>(hi16<Tag>(a.x), lo16<Tag>(a.x), s, r, fin) |
+            (quant_pair<FMT>(hi16<Tag>(a.y), lo16<Tag>(a.y), s, r, fin) << 16);
+      o.y = quant_pair<FMT>(hi16<Tag>(a.z), lo16<Tag>(a.z), s, r, fin) |
+            (quant_pair<FMT>(hi16<Tag>(a.w), lo16<Tag>(a.w), s, r, fin) << 16);
+      st_stream(q8 + v, o);
+    }
+    for (int64_t i = head + nv * 8 + tid; i < n; i += nthreads)
+      q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
+  } else {
+    for (int64_t i = tid; i < n; i += nthreads) q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
+  }
+}
+
+// ---- launch helpers ---------------------------------------------------------
+template <typename K>
+static int64_t persistent_grid(K kernel, int64_t work_items_per_cta_slot, int64_t n_items) {
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kQuantThreads, 0);
+  if (occ < 1) occ = 1;
+  int64_t grid = (int64_t)sm_count() * occ;
+  const int64_t need = (n_items + work_items_per_cta_slot - 1) / work_items_per_cta_slot;
+  if (grid > need) grid = need;
+  return grid < 1 ? 1 : grid;
+}
+
+template <int DT, int FMT>
+static cudaError_t quant_1x128_t(const void* x, int64_t R, int64_t C, uint8_t* q, float* scales,
+                                 cudaStream_t st) {
+  const int64_t n_tiles = R * (C / 128);
+  const uintptr_t xa = (uintptr_t)x, qa = (uintptr_t)q;
+  if constexpr (DT != GS_F32) {
+    if ((xa & 15u) == 0 && (qa & 7u) == 0) {
+      using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
+      auto k = quant_1x128_v16<Tag, FMT>;
+      // 16 tiles (8 warps x 2) per CTA per unrolled slot
+      const int64_t grid = persistent_grid(k, (kQuantThreads / 16) * kQuantUnroll, n_tiles);
+      k<<<(unsigned)grid, kQuantThreads, 0, st>>>(reinterpret_cast<const uint4*>(x), n_tiles,
+                                                   reinterpret_cast<uint2*>(q), scales);
+      return cudaGetLastError();
+    }
+  } else {
+    if ((xa & 15u) == 0 && (qa & 3u) == 0) {
+      auto k = quant_1x128_v32<FMT>;
+      const int64_t grid = persistent_grid(k, kQuantThreads / 32, n_tiles);
+      k<<<(unsigned)grid, kQuantThreads, 0, st>>>(reinterpret_cast<const uint4*>(x), n_tiles,
+                                                  reinterpret_cast<uint32_t*>(q), scales);
+      return cudaGetLastError();
+    }
+  }
+  auto k = quant_1x128_any<DT, FMT>;
+  const int64_t grid = persistent_grid(k, kQuantThreads / 32, n_tiles);
+  k<<<(unsigned)grid, kQuantThreads, 0, st>>>(x, n_tiles, q, scales);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t quant_1x128_f(const void* x, int dt, int64_t R, int64_t C, uint8_t* q,
+                                 float* scales, cudaStream_t st) {
+  if (dt == GS_BF16) return quant_1x128_t<GS_BF16, FMT>(x, R, C, q, scales, st);
+  if (dt == GS_F16) return quant_1x128_t<GS_F16, FMT>(x, R, C, q, scales, st);
+  return quant_1x128_t<GS_F32, FMT>(x, R, C, q, scales, st);
+}
+
+cudaError_t launch_quant_1x128(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
+                               float* scales, cudaStream_t stream) {
+  if (R == 0 || C == 0) return cudaSuccess;
+  return fmt == GS_E4M3 ? quant_1x128_f<GS_E4M3>(x, dtype, R, C, q, scales, stream)
+                        : quant_1x128_f<GS_E5M2>(x, dtype, R, C, q, scales, stream);
+}
+
+template <int DT, int FMT>
+cudaError_t quant_128x128_simple_t(const void* x, int64_t R, int64_t C, uint8_t* q, float* scales,
+                                   cudaStream_t st) {
+  auto k = quant_128x128_any<DT, FMT>;
+  const int64_t grid = persistent_grid(k, 1, (R / 128) * (C / 128));
+  k<<<(unsigned)grid, kQuantThreads, 0, st>>>(x, R, C, q, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_128x128_simple(const void* x, int dtype, int64_t R, int64_t C, int fmt,
+                                        uint8_t* q, float* scales, cudaStream_t st) {
+  if (R == 0 || C == 0) return cudaSuccess;
+  if (fmt == GS_E4M3) {
+    if (dtype == GS_BF16) return quant_128x128_simple_t<GS_BF16, GS_E4M3>(x, R, C, q, scales, st);
+    if (dtype == GS_F16) return quant_128x128_simple_t<GS_F16, GS_E4M3>(x, R, C, q, scales, st);
+    return quant_128x128_simple_t<GS_F32, GS_E4M3>(x, R, C, q, scales, st);
+  }
+  if (dtype == GS_BF16) return quant_128x128_simple_t<GS_BF16, GS_E5M2>(x, R, C, q, scales, st);
+  if (dtype == GS_F16) return quant_128x128_simple_t<GS_F16, GS_E5M2>(x, R, C, q, scales, st);
+  return quant_128x128_simple_t<GS_F32, GS_E5M2>(x, R, C, q, scales, st);
+}
+
+template <int DT, int FMT>
+static cudaError_t quant_tensor_t(const void* x, int64_t n, uint8_t* q, float* scale,
+                                  uint32_t* partials, cudaStream_t st) {
+  auto k1 = amax_partials<DT>;
+  auto k2 = quant_tensor_pass2<DT, FMT>;
+  int64_t g1 = persistent_grid(k1, kQuantThreads * 8, n);
+  if (g1 > kMaxAmaxBlocks) g1 = kMaxAmaxBlocks;
+  k1<<<(unsigned)g1, kQuantThreads, 0, st>>>(x, n, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t g2 = persistent_grid(k2, kQuantThreads * 8, n);
+  k2<<<(unsigned)g2, kQuantThreads, 0, st>>>(x, n, q, scale, partials, (int)g1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tensor(const void* x, int dtype, int64_t n, int fmt, uint8_t* q,
+                                float* scale, uint32_t* partials, cudaStream_t st) {
+  if (fmt == GS_E4M3) {
+    if (dtype == GS_BF16) return quant_tensor_t<GS_BF16, GS_E4M3>(x, n, q, scale, partials, st);
+    if (dtype == GS_F16) return quant_tensor_t<GS_F16, GS_E4M3>(x, n, q, scale, partials, st);
+    return quant_tensor_t<GS_F32, GS_E4M3>(x, n, q, scale, partials, st);
+  }
+  if (dtype == GS_BF16) return quant_tensor_t<GS_BF16, GS_E5M2>(x, n, q, scale, partials, st);
+  if (dtype == GS_F16) return quant_tensor_t<GS_F16, GS_E5M2>(x, n, q, scale, partials, st);
+  return quant_tensor_t<GS_F32, GS_E5M2>(x, n, q, scale, partials, st);
+}
+
+}  // namespace gs

@@ -1,0 +1,217 @@
+// fp8_quant_tma.cu -- 128x128 block-scaled FP8 quantisation of 16-bit
+// weights with TMA staging ("Loss scaling, FP8, and the failure that never
+// crashes", section "FP8 needs a finer-grained fix than a single scale
+// factor", and "Mixed precision and FP8 training", section "FP8 training":
+// one FP32 scale per 128x128 weight block).
+//
+// A persistent CTA walks its share of the blocks.  One elected thread
+// issues cp.async.bulk.tensor.2d loads of whole 128x128 tiles (32 KB,
+// no swizzle, no multicast) into a 3-stage ring, each stage guarded by an
+// mbarrier with a transaction count.  All 256 threads then pull the tile
+// from shared memory into registers (8 x 16 B each, conflict-free rows of
+// 256 B), reduce the block amax (packed 16-bit max, warp shuffle, one word
+// per warp), release the stage so the next load overlaps the cast, and
+// write FP8 codes straight from registers with 8-byte coalesced stores.
+// Every wait on an mbarrier is bounded by %globaltimer; a CTA that gives
+// up records GS_ERR_TIMEOUT in the device status word, waits (bounded) for
+// its own loads still in flight, and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+constexpr int kTmaThreads = 256;
+constexpr int kTmaStages = 3;
+constexpr int kTileBytes = 128 * 128 * 2;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kTmaSmemBytes = kTmaStages * kTileBytes + kTmaStages * 8 + 2 * 8 * 4 + 64;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+__device__ __forceinline__ void tma_load_tile(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                              int32_t col, int32_t row) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(kTileBytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(col), "r"(row), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <typename Tag, int FMT>
+__global__ void __launch_bounds__(kTmaThreads)
+    quant_128x128_tma(const __grid_constant__ CUtensorMap map, int64_t nbr, int64_t nbc,
+                      uint8_t* __restrict__ q, int64_t C, float* __restrict__ scales,
+                      int32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kTileBytes);
+  uint32_t* red = reinterpret_cast<uint32_t*>(full + kTmaStages);  // [2][8]
+
+  const int64_t n_blocks = nbr * nbc;
+  if ((int64_t)blockIdx.x >= n_blocks) return;
+  const int64_t my_n = (n_blocks - 1 - blockIdx.x) / gridDim.x + 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int64_t k) {
+    const int64_t b = blockIdx.x + k * gridDim.x;
+    tma_load_tile(&map, &full[k % kTmaStages], tiles + (k % kTmaStages) * kTileBytes,
+                  (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * 128));
+  };
+  int64_t issued = 0;
+  if (tid == 0)
+    for (; issued < kTmaStages && issued < my_n; ++issued) issue(issued);
+
+  // Thread tid owns rows (tid >> 4) + 16 j, 16-byte column chunk (tid & 15).
+  const int row0 = tid >> 4, chunk = tid & 15;
+  for (int64_t k = 0; k < my_n; ++k) {
+    const int stage = (int)(k % kTmaStages);
+    const bool ok = mbar_wait_bounded(&full[stage], (uint32_t)((k / kTmaStages) & 1));
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicExch(status, (int32_t)GS_ERR_TIMEOUT);
+        // let the loads of this CTA still in flight land before exiting
+        for (int64_t j = k; j < issued; ++j)
+          (void)mbar_wait_bounded(&full[j % kTmaStages], (uint32_t)((j / kTmaStages) & 1));
+      }
+      __syncthreads();
+      return;
+    }
+    const uint4* tile = reinterpret_cast<const uint4*>(tiles + stage * kTileBytes);
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = tile[(row0 + 16 * j) * 16 + chunk];
+    const uint32_t mm = 0x7FFF7FFFu;
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v[j].x & mm, v[j].y & mm), __vmaxu2(v[j].z & mm, v[j].w & mm)));
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    uint32_t* rb = red + (k & 1) * 8;
+    if (lane == 0) rb[warp] = m;
+    __syncthreads();  // every thread holds its part of the tile: the stage is free
+    if (tid == 0 && issued < my_n) issue(issued++);
+    m = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m = max(m, rb[w]);
+    const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
+    const bool fin = isfinite(s);
+    const float r = __frcp_rn(s);
+    const int64_t b = blockIdx.x + k * gridDim.x;
+    const int64_t r0 = (b / nbc) * 128, c0 = (b % nbc) * 128;
+    if (tid == 0) scales[b] = s;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint2 o;
+      o.x = quant_pair<FMT>(hi16<Tag>(v[j].x), lo16<Tag>(v[j].x), s, r, fin) |
+            (quant_pair<FMT>(hi16<Tag>(v[j].y), lo16<Tag>(v[j].y), s, r, fin) << 16);
+      o.y = quant_pair<FMT>(hi16<Tag>(v[j].z), lo16<Tag>(v[j].z), s, r, fin) |
+            (quant_pair<FMT>(hi16<Tag>(v[j].w), lo16<Tag>(v[j].w), s, r, fin) << 16);
+      st_stream(reinterpret_cast<uint2*>(q + (r0 + row0 + 16 * j) * C + c0 + chunk * 8), o);
+    }
+  }
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+cudaError_t launch_quant_128x128_simple(const void* x, int dtype, int64_t R, int64_t C, int fmt,
+                                        uint8_t* q, float* scales, cudaStream_t st);
+
+template <typename Tag, int FMT>
+static cudaError_t launch_tma_t(const CUtensorMap& map, int64_t R, int64_t C, uint8_t* q,
+                                float* scales, int32_t* status, cudaStream_t st) {
+  auto k = quant_128x128_tma<Tag, FMT>;
+  static int occ = 0;
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kTmaThreads, kTmaSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+  }
+  const int64_t nbr = R / 128, nbc = C / 128;
+  int64_t grid = (int64_t)sm_count() * occ;
+  if (grid > nbr * nbc) grid = nbr * nbc;
+  k<<<(unsigned)grid, kTmaThreads, kTmaSmemBytes, st>>>(map, nbr, nbc, q, C, scales, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_128x128(const void* x, int dtype, int64_t R, int64_t C, int fmt,
+                                 uint8_t* q, float* scales, int32_t* status, cudaStream_t st) {
+  if (R == 0 || C == 0) return cudaSuccess;
+  const bool tma_ok = dtype != GS_F32 && ((uintptr_t)x & 15u) == 0 && ((uintptr_t)q & 7u) == 0 &&
+                      R < (int64_t(1) << 31) && C < (int64_t(1) << 31) && encode_fn() != nullptr;
+  if (!tma_ok) return launch_quant_128x128_simple(x, dtype, R, C, fmt, q, scales, st);
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)R};
+  const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult cr = encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(x), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return launch_quant_128x128_simple(x, dtype, R, C, fmt, q, scales, st);
+  if (fmt == GS_E4M3)
+    return dtype == GS_BF16 ? launch_tma_t<BF16Tag, GS_E4M3>(map, R, C, q, scales, status, st)
+                            : launch_tma_t<F16Tag, GS_E4M3>(map, R, C, q, scales, status, st);
+  return dtype == GS_BF16 ? launch_tma_t<BF16Tag, GS_E5M2>(map, R, C, q, scales, status, st)
+                          : launch_tma_t<F16Tag, GS_E5M2>(map, R, C, q, scales, status, st);
+}
+
+}  // namespace gs

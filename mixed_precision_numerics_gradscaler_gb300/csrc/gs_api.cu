@@ -1,0 +1,306 @@
+// gs_api.cu -- the C ABI declared in include/gsfp8.h: argument validation
+// on the host (nothing is launched unless every check passes), the
+// gradient-list chunk table, status codes and launch dispatch.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cmath>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "gs_internal.h"
+#include "gsfp8.h"
+
+// The device status word (GS_OK or GS_ERR_TIMEOUT), one per device.
+__device__ int32_t g_gs_device_status = 0;
+
+struct gs_tensor_list {
+  int device;
+  gs::Chunk* d_chunks;
+  int64_t n_chunks;
+  int64_t total;
+  gs::ListWs* d_ws;
+};
+
+namespace gs {
+
+static thread_local int t_last_cuda_error = 0;
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
+int sm_count() {
+  static int cache[kMaxDevices] = {0};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 1;
+  if (cache[d] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    cache[d] = n > 0 ? n : 1;
+  }
+  return cache[d];
+}
+
+static int32_t* device_status_ptr() {
+  static int32_t* cache[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gs_device_status) != cudaSuccess) return nullptr;
+    cache[d] = static_cast<int32_t*>(p);
+  }
+  return cache[d];
+}
+
+static int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return GS_ERR_CUDA;
+}
+
+// A pointer the current device can dereference: device memory of this
+// device, managed memory, or mapped (registered) host memory.
+static bool device_reachable(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of the query
+    return false;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      return a.device == current_device();
+    case cudaMemoryTypeManaged:
+      return true;
+    case cudaMemoryTypeHost:
+      return a.devicePointer != nullptr;
+    default:
+      return false;
+  }
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return na && nb && x < y + nb && y < x + na;
+}
+
+static size_t dtype_size(int dt) { return dt == GS_F32 ? 4 : 2; }
+static bool valid_dtype(int dt) { return dt == GS_F16 || dt == GS_BF16 || dt == GS_F32; }
+static bool valid_fmt(int f) { return f == GS_E4M3 || f == GS_E5M2; }
+
+static bool mul_ok(int64_t a, int64_t b) { return a >= 0 && b >= 0 && (b == 0 || a <= INT64_MAX / b); }
+
+}  // namespace gs
+
+using namespace gs;
+
+extern "C" {
+
+const char* gs_status_str(int status) {
+  switch (status) {
+    case GS_OK: return "GS_OK";
+    case GS_ERR_NULL: return "GS_ERR_NULL: a required pointer is NULL";
+    case GS_ERR_SHAPE: return "GS_ERR_SHAPE: invalid sizes or block shape";
+    case GS_ERR_DTYPE: return "GS_ERR_DTYPE: unsupported element type or FP8 format";
+    case GS_ERR_ARG: return "GS_ERR_ARG: invalid argument";
+    case GS_ERR_CUDA: return "GS_ERR_CUDA: a CUDA call failed";
+    case GS_ERR_TIMEOUT: return "GS_ERR_TIMEOUT: a bounded device-side wait expired";
+    default: return "unknown gs_status";
+  }
+}
+
+int gs_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* gs_version(void) { return "gsfp8 0.1.0 (sm_103a)"; }
+
+int gs_tensor_list_create(const void* const* grads, void* const* outs, const int64_t* numels,
+                          int32_t n_tensors, gs_tensor_list** out) {
+  if (!out) return GS_ERR_NULL;
+  *out = nullptr;
+  if (n_tensors < 0) return GS_ERR_SHAPE;
+  if (n_tensors > 0 && (!grads || !outs || !numels)) return GS_ERR_NULL;
+  std::vector<Chunk> chunks;
+  int64_t total = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t n = numels[i];
+    if (n < 0 || n > (INT64_MAX >> 3)) return GS_ERR_SHAPE;
+    if (n == 0) continue;
+    if (!grads[i] || !outs[i]) return GS_ERR_NULL;
+    if (!aligned(grads[i], 2) || !aligned(outs[i], 4)) return GS_ERR_ARG;
+    if (!device_reachable(grads[i]) || !device_reachable(outs[i])) return GS_ERR_ARG;
+    if (overlaps(grads[i], (size_t)n * 2, outs[i], (size_t)n * 4)) return GS_ERR_ARG;
+    const uint16_t* g = static_cast<const uint16_t*>(grads[i]);
+    float* o = static_cast<float*>(outs[i]);
+    for (int64_t off = 0; off < n; off += kChunkElems)
+      chunks.push_back(Chunk{g + off, o + off, (n - off) < kChunkElems ? (n - off) : kChunkElems});
+    total += n;
+  }
+  gs_tensor_list* l = new (std::nothrow) gs_tensor_list{current_device(), nullptr, 0, total, nullptr};
+  if (!l) return GS_ERR_ARG;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&l->d_ws), sizeof(ListWs));
+  if (e == cudaSuccess) e = cudaMemset(l->d_ws, 0, sizeof(ListWs));
+  if (e == cudaSuccess && !chunks.empty()) {
+    e = cudaMalloc(reinterpret_cast<void**>(&l->d_chunks), chunks.size() * sizeof(Chunk));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(l->d_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
+                     cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    if (l->d_chunks) cudaFree(l->d_chunks);
+    if (l->d_ws) cudaFree(l->d_ws);
+    delete l;
+    return cuda_fail(e);
+  }
+  l->n_chunks = (int64_t)chunks.size();
+  *out = l;
+  return GS_OK;
+}
+
+int gs_tensor_list_destroy(gs_tensor_list* list) {
+  if (!list) return GS_OK;
+  int prev = current_device();
+  cudaSetDevice(list->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (list->d_chunks) cudaFree(list->d_chunks);
+  if (list->d_ws) cudaFree(list->d_ws);
+  cudaSetDevice(prev);
+  delete list;
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_tensor_list_info(const gs_tensor_list* list, int64_t* total_elems, int64_t* n_chunks) {
+  if (!list) return GS_ERR_NULL;
+  if (total_elems) *total_elems = list->total;
+  if (n_chunks) *n_chunks = list->n_chunks;
+  return GS_OK;
+}
+
+int gs_unscale_check_update(const gs_tensor_list* list, float* scale, int32_t* growth_tracker,
+                            int32_t* found_inf, int64_t* skipped, float growth_factor,
+                            float backoff_factor, int32_t growth_interval, void* stream) {
+  if (!list || !scale || !growth_tracker || !found_inf) return GS_ERR_NULL;
+  if (growth_interval < 1) return GS_ERR_ARG;
+  if (!std::isfinite(growth_factor) || !(growth_factor > 0.0f) || !std::isfinite(backoff_factor) ||
+      !(backoff_factor > 0.0f))
+    return GS_ERR_ARG;
+  if (list->device != current_device()) return GS_ERR_ARG;
+  if (!aligned(scale, 4) || !aligned(growth_tracker, 4) || !aligned(found_inf, 4) ||
+      (skipped && !aligned(skipped, 8)))
+    return GS_ERR_ARG;
+  if (!device_reachable(scale) || !device_reachable(growth_tracker) || !device_reachable(found_inf) ||
+      (skipped && !device_reachable(skipped)))
+    return GS_ERR_ARG;
+  cudaError_t e = launch_unscale_check_update(list->d_chunks, list->n_chunks, list->d_ws, scale,
+                                              growth_tracker, found_inf, skipped, growth_factor,
+                                              backoff_factor, growth_interval,
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_scaler_state_get(const float* scale, const int32_t* growth_tracker, float* h_scale,
+                        int32_t* h_growth_tracker, void* stream) {
+  if (!scale || !growth_tracker || !h_scale || !h_growth_tracker) return GS_ERR_NULL;
+  if (!device_reachable(scale) || !device_reachable(growth_tracker)) return GS_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h_scale, scale, sizeof(float), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h_growth_tracker, growth_tracker, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_scaler_state_set(float* scale, int32_t* growth_tracker, float h_scale,
+                        int32_t h_growth_tracker, void* stream) {
+  if (!scale || !growth_tracker) return GS_ERR_NULL;
+  if (h_growth_tracker < 0) return GS_ERR_ARG;
+  if (!device_reachable(scale) || !device_reachable(growth_tracker)) return GS_ERR_ARG;
+  cudaError_t e = launch_set_state(scale, growth_tracker, h_scale, h_growth_tracker,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int fp8_quant_block(const void* x, int in_dtype, int64_t R, int64_t C, int32_t block_r,
+                    int32_t block_c, int fmt, uint8_t* q, float* scales, void* stream) {
+  if (!valid_dtype(in_dtype) || !valid_fmt(fmt)) return GS_ERR_DTYPE;
+  if (R < 0 || C < 0 || !mul_ok(R, C) || !mul_ok(R * C, 4)) return GS_ERR_SHAPE;
+  if (!((block_r == 1 || block_r == 128) && block_c == 128)) return GS_ERR_SHAPE;
+  if (R % block_r != 0 || C % block_c != 0) return GS_ERR_SHAPE;
+  if (R == 0 || C == 0) return GS_OK;
+  if (!x || !q || !scales) return GS_ERR_NULL;
+  const size_t n = (size_t)(R * C), esz = dtype_size(in_dtype);
+  const size_t nscales = (size_t)((R / block_r) * (C / block_c));
+  if (!aligned(x, esz) || !aligned(scales, 4)) return GS_ERR_ARG;
+  if (!device_reachable(x) || !device_reachable(q) || !device_reachable(scales)) return GS_ERR_ARG;
+  if (overlaps(x, n * esz, q, n) || overlaps(x, n * esz, scales, nscales * 4) ||
+      overlaps(q, n, scales, nscales * 4))
+    return GS_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = block_r == 1
+                      ? launch_quant_1x128(x, in_dtype, R, C, fmt, q, scales, st)
+                      : launch_quant_128x128(x, in_dtype, R, C, fmt, q, scales,
+                                             device_status_ptr(), st);
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+size_t gs_ws_bytes(void) { return (size_t)kMaxAmaxBlocks * sizeof(uint32_t); }
+
+int fp8_quant_tensor(const void* x, int in_dtype, int64_t n, int fmt, uint8_t* q, float* scale,
+                     void* ws, void* stream) {
+  if (!valid_dtype(in_dtype) || !valid_fmt(fmt)) return GS_ERR_DTYPE;
+  if (n < 0 || !mul_ok(n, 4)) return GS_ERR_SHAPE;
+  if (!scale || !ws || (n > 0 && (!x || !q))) return GS_ERR_NULL;
+  const size_t esz = dtype_size(in_dtype);
+  if (!aligned(scale, 4) || !aligned(ws, 4) || (n > 0 && !aligned(x, esz))) return GS_ERR_ARG;
+  if (!device_reachable(scale) || !device_reachable(ws) ||
+      (n > 0 && (!device_reachable(x) || !device_reachable(q))))
+    return GS_ERR_ARG;
+  if (overlaps(x, (size_t)n * esz, q, (size_t)n) || overlaps(ws, gs_ws_bytes(), x, (size_t)n * esz) ||
+      overlaps(ws, gs_ws_bytes(), q, (size_t)n) || overlaps(scale, 4, q, (size_t)n) ||
+      overlaps(scale, 4, x, (size_t)n * esz) || overlaps(scale, 4, ws, gs_ws_bytes()))
+    return GS_ERR_ARG;
+  cudaError_t e = launch_quant_tensor(x, in_dtype, n, fmt, q, scale, static_cast<uint32_t*>(ws),
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int fp8_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C, int32_t block_r,
+                int32_t block_c, int fmt, int out_dtype, void* y, void* stream) {
+  if (!valid_fmt(fmt) || !(out_dtype == GS_F32 || out_dtype == GS_BF16)) return GS_ERR_DTYPE;
+  if (R < 0 || C < 0 || !mul_ok(R, C) || !mul_ok(R * C, 4)) return GS_ERR_SHAPE;
+  const bool per_tensor = (int64_t)block_r == R && (int64_t)block_c == C;
+  const bool blocked = (block_r == 1 || block_r == 128) && block_c == 128;
+  if (!per_tensor && !blocked) return GS_ERR_SHAPE;
+  if (!per_tensor && (R % block_r != 0 || C % block_c != 0)) return GS_ERR_SHAPE;
+  if (R == 0 || C == 0) return GS_OK;
+  if (!q || !scales || !y) return GS_ERR_NULL;
+  const size_t n = (size_t)(R * C), ysz = out_dtype == GS_F32 ? 4 : 2;
+  const size_t nscales = per_tensor ? 1 : (size_t)((R / block_r) * (C / block_c));
+  if (!aligned(scales, 4) || !aligned(y, ysz)) return GS_ERR_ARG;
+  if (!device_reachable(q) || !device_reachable(scales) || !device_reachable(y)) return GS_ERR_ARG;
+  if (overlaps(y, n * ysz, q, n) || overlaps(y, n * ysz, scales, nscales * 4)) return GS_ERR_ARG;
+  cudaError_t e = launch_dequant(q, scales, R, C, block_r, block_c, fmt, out_dtype, y,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_device_status(int32_t* h_status, void* stream) {
+  if (!h_status) return GS_ERR_NULL;
+  int32_t* p = device_status_ptr();
+  if (!p) return cuda_fail(cudaGetLastError());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h_status, p, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+}  // extern "C"

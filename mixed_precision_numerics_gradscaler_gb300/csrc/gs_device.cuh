@@ -1,0 +1,165 @@
+// gs_device.cuh -- device-side building blocks shared by the kernels:
+// FP8 pack/unpack through the sm_89+ cvt instructions, 16-bit float
+// unpacking, the exact fp32 quotient used by the quantiser, and the
+// library's device status word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "gsfp8.h"
+
+namespace gs {
+
+// Largest finite magnitudes of the two OCP FP8 encodings ("Numerical
+// Precision, Mixed Precision, and Loss Scaling", paragraph on the FP8
+// specification).
+template <int FMT>
+struct Fp8Max;
+template <>
+struct Fp8Max<GS_E4M3> {
+  static constexpr float value = 448.0f;
+};
+template <>
+struct Fp8Max<GS_E5M2> {
+  static constexpr float value = 57344.0f;
+};
+
+// Floor applied to every block amax before dividing by MAX ("Mixed
+// precision and FP8 training", section "FP8 training": clamp(min=1e-12)).
+constexpr float kAmaxFloor = 1e-12f;
+
+// Canonical FP8 NaN written for every NaN input.
+constexpr uint32_t kFp8NaN = 0x7Fu;
+
+// ---- FP8 conversions ------------------------------------------------------
+// cvt.rn.satfinite.{e4m3x2,e5m2x2}.f32 d, a, b: a -> high byte, b -> low
+// byte, round to nearest even, magnitudes beyond the format's max (and
+// +-Inf) saturate to +-max.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_f32x2_fp8x2(float hi, float lo) {
+  uint16_t d;
+  if constexpr (FMT == GS_E4M3) {
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  } else {
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  }
+  return d;
+}
+
+// Two FP8 codes (low byte first) -> two exact f16 values packed in a word.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x2_f16x2(uint16_t codes) {
+  uint32_t d;
+  if constexpr (FMT == GS_E4M3) {
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(codes));
+  } else {
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(d) : "h"(codes));
+  }
+  return d;
+}
+
+// Two fp32 values -> two bfloat16 (round to nearest even), hi in the high
+// half of the word.
+__device__ __forceinline__ uint32_t cvt_f32x2_bf16x2(float hi, float lo) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// ---- 16-bit float unpacking (exact) ---------------------------------------
+struct BF16Tag {};
+struct F16Tag {};
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float lo_f16(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float hi_f16(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+template <typename Tag>
+__device__ __forceinline__ float lo16(uint32_t w) {
+  if constexpr (std::is_same<Tag, BF16Tag>::value) return lo_bf16(w);
+  else return lo_f16(w);
+}
+template <typename Tag>
+__device__ __forceinline__ float hi16(uint32_t w) {
+  if constexpr (std::is_same<Tag, BF16Tag>::value) return hi_bf16(w);
+  else return hi_f16(w);
+}
+
+// Magnitude bit pattern of a 16-bit float held in the low 16 bits -> float.
+// For both BF16 and FP16, the unsigned order of magnitude patterns is the
+// order of |x|, with Inf above every finite value and NaN above Inf, so an
+// integer max over patterns is a NaN-propagating amax.
+template <typename Tag>
+__device__ __forceinline__ float mag16_to_float(uint32_t m) {
+  if constexpr (std::is_same<Tag, BF16Tag>::value) return __uint_as_float(m << 16);
+  else return __half2float(__ushort_as_half((unsigned short)m));
+}
+
+// ---- scale and exact quotient ---------------------------------------------
+// s = max(amax, 1e-12) / MAX in fp32; a NaN amax stays NaN.
+template <int FMT>
+__device__ __forceinline__ float block_scale(float amax) {
+  float a = (amax < kAmaxFloor) ? kAmaxFloor : amax;  // false for NaN: NaN kept
+  return __fdiv_rn(a, Fp8Max<FMT>::value);
+}
+
+// Correctly rounded fp32 quotient x / s for finite s > 0 (normal) given
+// r = RN(1/s), from one product and two residual corrections (Markstein's
+// theorem, P. Markstein, "IA-64 and Elementary Functions", 2000; also
+// Muller et al., "Handbook of Floating-Point Arithmetic", ch. 4): after the
+// first correction the estimate is within one ulp of x / s, so the second
+// correction returns the correctly rounded quotient.  The residuals
+// x - q*s are exact (fused multiply-add) whenever |x / s| is large enough
+// to matter to an FP8 code (>= 2^-17 with s >= 2^-49), and the sign of a
+// zero result is taken from x, as IEEE division does for s > 0.
+__device__ __forceinline__ float exact_quotient(float x, float s, float r) {
+  float q = __fmul_rn(x, r);
+  float e = __fmaf_rn(-q, s, x);
+  q = __fmaf_rn(e, r, q);
+  e = __fmaf_rn(-q, s, x);
+  q = __fmaf_rn(e, r, q);
+  return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// Quantise a pair with a finite scale (fast path) or a non-finite one (a
+// block holding Inf or NaN: IEEE division, NaN codes forced to 0x7F).
+template <int FMT>
+__device__ __forceinline__ uint32_t quant_pair(float hi, float lo, float s, float r,
+                                               bool finite_scale) {
+  if (finite_scale) return cvt_f32x2_fp8x2<FMT>(exact_quotient(hi, s, r), exact_quotient(lo, s, r));
+  float qh = __fdiv_rn(hi, s), ql = __fdiv_rn(lo, s);
+  uint32_t c = cvt_f32x2_fp8x2<FMT>(qh, ql);
+  if (qh != qh) c = (c & 0x00FFu) | (kFp8NaN << 8);
+  if (ql != ql) c = (c & 0xFF00u) | kFp8NaN;
+  return c;
+}
+
+// ---- streaming memory access ----------------------------------------------
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
+  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_stream(uint2* p, uint2 v) {
+  asm volatile("st.global.L1::no_allocate.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y)
+               : "memory");
+}
+
+}  // namespace gs

@@ -1,0 +1,54 @@
+// gs_internal.h -- host-side declarations shared by the library's
+// translation units (kernel launchers, the chunk table, device queries).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gs {
+
+// One contiguous run of a gradient tensor: at most kChunkElems elements.
+// Chunk starts are multiples of kChunkElems from the tensor's start, so
+// every chunk of a tensor keeps the tensor's alignment.
+struct Chunk {
+  const uint16_t* in;  // scaled FP16 gradients
+  float* out;          // FP32 unscaled output
+  int64_t n;
+};
+constexpr int64_t kChunkElems = 32768;
+
+// Per-list device workspace of the last-CTA epilogue.  Both words return
+// to zero at the end of every call.
+struct ListWs {
+  unsigned int arrived;
+  int32_t found;
+  int32_t pad[2];
+};
+
+// Cached device properties of the current device.
+int sm_count();
+int current_device();
+
+// Launchers.  Each returns the launch's cudaError_t.
+cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks, ListWs* ws,
+                                        float* scale, int32_t* tracker, int32_t* found,
+                                        int64_t* skipped, float growth, float backoff,
+                                        int32_t interval, cudaStream_t stream);
+
+cudaError_t launch_quant_1x128(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
+                               float* scales, cudaStream_t stream);
+cudaError_t launch_quant_128x128(const void* x, int dtype, int64_t R, int64_t C, int fmt,
+                                 uint8_t* q, float* scales, int32_t* status,
+                                 cudaStream_t stream);
+cudaError_t launch_quant_tensor(const void* x, int dtype, int64_t n, int fmt, uint8_t* q,
+                                float* scale, uint32_t* partials, cudaStream_t stream);
+cudaError_t launch_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C,
+                           int block_r, int block_c, int fmt, int out_dtype, void* y,
+                           cudaStream_t stream);
+cudaError_t launch_set_state(float* scale, int32_t* tracker, float h_scale, int32_t h_tracker,
+                             cudaStream_t stream);
+
+// Number of per-CTA amax partials the per-tensor path may write.
+constexpr int kMaxAmaxBlocks = 2048;
+
+}  // namespace gs

@@ -1,0 +1,151 @@
+// unscale_check.cu -- one GradScaler step over a whole gradient list in a
+// single launch ("Loss scaling, FP8, and the failure that never crashes",
+// section "Loss scaling, derived from the chain rule you already have",
+// and its SimpleGradScaler listing; "Numerical Precision, Mixed Precision,
+// and Loss Scaling", GradScaler defaults paragraph and steps 4 and 6 of its
+// training step):
+//   out = fp32(g) * fp32(1/S) for every element of every tensor,
+//   found_inf = any scaled FP16 input with an all-ones exponent field,
+//   then S / growth tracker updated on the device by the last CTA to finish.
+//
+// Layout: a persistent grid walks the list's chunk table (32 Ki-element
+// chunks, grid-stride).  Each thread moves 16-byte vectors: 8 FP16 in, 2 x 4
+// FP32 out, several vectors in flight per thread.  HBM-bound: 6 bytes per
+// element (2 read + 4 written).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+constexpr int kUnscaleThreads = 256;
+constexpr int kUnscaleUnroll = 4;
+
+// 0xFFFF in each 16-bit lane whose exponent field is all ones (Inf / NaN).
+__device__ __forceinline__ uint32_t nonfinite2(uint32_t w) {
+  return __vcmpeq2(w & 0x7C007C00u, 0x7C007C00u);
+}
+
+__device__ __forceinline__ void unscale8(uint4 v, float inv, uint4* out, uint32_t& bad) {
+  bad |= nonfinite2(v.x) | nonfinite2(v.y) | nonfinite2(v.z) | nonfinite2(v.w);
+  uint4 a, b;
+  a.x = __float_as_uint(__fmul_rn(lo_f16(v.x), inv));
+  a.y = __float_as_uint(__fmul_rn(hi_f16(v.x), inv));
+  a.z = __float_as_uint(__fmul_rn(lo_f16(v.y), inv));
+  a.w = __float_as_uint(__fmul_rn(hi_f16(v.y), inv));
+  b.x = __float_as_uint(__fmul_rn(lo_f16(v.z), inv));
+  b.y = __float_as_uint(__fmul_rn(hi_f16(v.z), inv));
+  b.z = __float_as_uint(__fmul_rn(lo_f16(v.w), inv));
+  b.w = __float_as_uint(__fmul_rn(hi_f16(v.w), inv));
+  st_stream(out, a);
+  st_stream(out + 1, b);
+}
+
+__device__ __forceinline__ void unscale1(const uint16_t* in, float* out, int64_t i, float inv,
+                                         uint32_t& bad) {
+  const uint32_t h = in[i];
+  bad |= ((h & 0x7C00u) == 0x7C00u);
+  out[i] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), inv);
+}
+
+__device__ __forceinline__ uint32_t unscale_chunk(const Chunk ch, float inv) {
+  const uint16_t* in = ch.in;
+  float* out = ch.out;
+  const int64_t n = ch.n;
+  uint32_t bad = 0;
+  // Scalar head until the input is 16-byte aligned; the vector body also
+  // needs the output 16-byte aligned at the same element, else all scalar.
+  int64_t head = (int64_t)(((16u - ((uint32_t)(uintptr_t)in & 15u)) & 15u) >> 1);
+  if (head > n) head = n;
+  if ((((uintptr_t)(out + head)) & 15u) != 0) head = n;
+  for (int64_t i = threadIdx.x; i < head; i += blockDim.x) unscale1(in, out, i, inv, bad);
+  const int64_t nv = (n - head) >> 3;
+  const uint4* in8 = reinterpret_cast<const uint4*>(in + head);
+  uint4* out4 = reinterpret_cast<uint4*>(out + head);
+  int64_t v = threadIdx.x;
+  for (; v + (kUnscaleUnroll - 1) * (int64_t)blockDim.x < nv; v += kUnscaleUnroll * blockDim.x) {
+    uint4 r[kUnscaleUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnscaleUnroll; ++u) r[u] = ld_stream(in8 + v + u * blockDim.x);
+#pragma unroll
+    for (int u = 0; u < kUnscaleUnroll; ++u) unscale8(r[u], inv, out4 + 2 * (v + u * blockDim.x), bad);
+  }
+  for (; v < nv; v += blockDim.x) unscale8(ld_stream(in8 + v), inv, out4 + 2 * v, bad);
+  for (int64_t i = head + nv * 8 + threadIdx.x; i < n; i += blockDim.x) unscale1(in, out, i, inv, bad);
+  return bad;
+}
+
+__global__ void __launch_bounds__(kUnscaleThreads)
+    unscale_check_update_kernel(const Chunk* __restrict__ chunks, int64_t n_chunks, ListWs* ws,
+                                float* scale, int32_t* tracker, int32_t* found_out,
+                                int64_t* skipped, float growth, float backoff, int32_t interval) {
+  // Every CTA reads S before it arrives below; the last CTA to arrive is the
+  // only writer, so all CTAs unscale with this step's S.
+  const float S = *scale;
+  const float inv = (float)(1.0 / (double)S);
+  uint32_t bad = 0;
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) bad |= unscale_chunk(chunks[c], inv);
+
+  const int any_bad = __syncthreads_or(bad != 0);
+  if (threadIdx.x != 0) return;
+  if (any_bad) atomicOr(&ws->found, 1);
+  __threadfence();
+  const unsigned int prev = atomicAdd(&ws->arrived, 1u);
+  if (prev != gridDim.x - 1) return;
+  // Last CTA: every flag is in; apply the control loop.
+  __threadfence();
+  const int32_t found = atomicOr(&ws->found, 0) != 0;
+  float s = *scale;
+  int32_t t = *tracker;
+  if (found) {
+    s = __fmul_rn(s, backoff);
+    t = 0;
+    if (skipped) *skipped += 1;
+  } else {
+    t += 1;
+    if (t >= interval) {
+      s = __fmul_rn(s, growth);
+      t = 0;
+    }
+  }
+  *scale = s;
+  *tracker = t;
+  *found_out = found;
+  ws->found = 0;
+  ws->arrived = 0;
+}
+
+cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks, ListWs* ws,
+                                        float* scale, int32_t* tracker, int32_t* found,
+                                        int64_t* skipped, float growth, float backoff,
+                                        int32_t interval, cudaStream_t stream) {
+  static int occ = 0;  // resident CTAs per SM (same on every GB300)
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, unscale_check_update_kernel, kUnscaleThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+  }
+  int64_t grid = (int64_t)sm_count() * occ;
+  if (grid > n_chunks) grid = n_chunks;
+  if (grid < 1) grid = 1;
+  unscale_check_update_kernel<<<(unsigned)grid, kUnscaleThreads, 0, stream>>>(
+      d_chunks, n_chunks, ws, scale, tracker, found, skipped, growth, backoff, interval);
+  return cudaGetLastError();
+}
+
+__global__ void set_state_kernel(float* scale, int32_t* tracker, float h_scale, int32_t h_tracker) {
+  *scale = h_scale;
+  *tracker = h_tracker;
+}
+
+cudaError_t launch_set_state(float* scale, int32_t* tracker, float h_scale, int32_t h_tracker,
+                             cudaStream_t stream) {
+  set_state_kernel<<<1, 1, 0, stream>>>(scale, tracker, h_scale, h_tracker);
+  return cudaGetLastError();
+}
+
+}  // namespace gs

@@ -111,7 +111,8 @@ def test_quant_matches_library_composition(orc, fmt, tdt):
     x[5, :128] = 0.0
     t = torch.from_numpy(x).view(R, C // 128, 128)
     mx = orc.fp8_max(fmt)
-    s = t.abs().amax(dim=-1, keepdim=True).clamp(min=1e-12) / mx
+    amax = t.abs().amax(dim=-1, keepdim=True).clamp(min=1e-12)
+    s = amax / torch.full_like(amax, mx)              # IEEE tensor / tensor division
     q_lib = (t / s).clamp(-mx, mx).to(tdt).view(torch.uint8).reshape(R, C).numpy()
     q, so = orc.quant_block(x, 1, 128, fmt)
     assert (so == s.reshape(R, C // 128).numpy()).all()
