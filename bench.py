@@ -59,6 +59,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--only", choices=["unscale", "quant_1x128", "dequant", "quant_128x128",
+                                      "quant_tensor"],
+                   help="time one kernel alone on a small case (for ncu captures)")
     return p.parse_args(argv)
 
 
@@ -526,12 +529,88 @@ def run_sweep(args):
     return 0
 
 
+def run_only(args):
+    """One kernel alone, on a case small enough for a full ncu capture: the
+    unscale on the first two layers of the Llama-3-8B list (18 tensors,
+    436 M elements: 0.87 GB in, 1.7 GB out); the FP8 kernels on their own
+    configs (268-470 MB of input)."""
+    import torch
+    import datagen as dg
+    from datagen import workloads as wl
+    import mixed_precision_numerics_gradscaler_gb300 as gs
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream().cuda_stream
+    dev = "cuda"
+    if args.only == "unscale":
+        cfg = wl.cfg2_grads()
+        n_t = 18
+        grads = [torch.empty(n, dtype=torch.float16, device=dev) for n in cfg.numels[:n_t]]
+        outs = [torch.empty(n, dtype=torch.float32, device=dev) for n in cfg.numels[:n_t]]
+        for t, g in enumerate(grads):
+            dg.fill_device(cfg.spec(t, 0), 0, g.numel(), g.data_ptr(), st)
+        tl = gs.gs_tensor_list_create(grads, outs)
+        sc = torch.tensor([65536.0], device=dev)
+        tr = torch.zeros(1, dtype=torch.int32, device=dev)
+        fi = torch.zeros(1, dtype=torch.int32, device=dev)
+        fn = lambda: gs.gs_unscale_check_update(tl, sc, tr, fi, None, 2.0, 0.5, 2000)
+        nbytes = 6 * sum(cfg.numels[:n_t])
+    elif args.only in ("quant_1x128", "dequant"):
+        a = wl.cfg3_act()
+        x = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
+        dg.fill_device(a.spec, 0, a.numel, x.data_ptr(), st)
+        q = torch.empty(a.rows, a.cols, dtype=torch.uint8, device=dev)
+        s = torch.empty(a.rows, a.cols // 128, dtype=torch.float32, device=dev)
+        y = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
+        gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)
+        if args.only == "quant_1x128":
+            fn = lambda: gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)
+        else:
+            fn = lambda: gs.fp8_dequant(q, s, 1, 128, "e4m3", y)
+        nbytes = 3 * a.numel + 4 * (a.numel // 128)
+    elif args.only == "quant_128x128":
+        w = wl.cfg4_weight()
+        x = torch.empty(w.rows, w.cols, dtype=torch.bfloat16, device=dev)
+        dg.fill_device(w.spec, 0, w.numel, x.data_ptr(), st)
+        q = torch.empty(w.rows, w.cols, dtype=torch.uint8, device=dev)
+        s = torch.empty(w.rows // 128, w.cols // 128, dtype=torch.float32, device=dev)
+        fn = lambda: gs.fp8_quant_block(x, 128, 128, "e4m3", q, s)
+        nbytes = 3 * w.numel + 4 * (w.numel // 16384)
+    else:
+        g = wl.cfg4_grad()
+        x = torch.empty(g.numel, dtype=torch.bfloat16, device=dev)
+        dg.fill_device(g.spec, 0, g.numel, x.data_ptr(), st)
+        q = torch.empty(g.numel, dtype=torch.uint8, device=dev)
+        s = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=dev)
+        fn = lambda: gs.fp8_quant_tensor(x, "e5m2", q, s, ws)
+        nbytes = 5 * g.numel + 4
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.median(ts)
+    peak, src = hbm_peak()
+    print(json.dumps({"only": args.only, "bytes": nbytes, "median_ms": ms, "gbs": nbytes / ms / 1e6,
+                      "frac": nbytes / ms / 1e6 / peak, "peak": peak, "peak_source": src,
+                      "steps": args.steps}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.only:
+        return run_only(args)
     return run_ours(args)
 
 

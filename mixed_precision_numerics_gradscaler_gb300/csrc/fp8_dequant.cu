@@ -68,6 +68,45 @@ __global__ void __launch_bounds__(kDeqThreads)
   }
 }
 
+// 32 codes per thread (one 32-byte load) -> 32 outputs (two or four 32-byte
+// stores); the 32 elements share one scale for every block shape (32 | 128).
+template <int KIND, int FMT, int OUT>
+__global__ void __launch_bounds__(kDeqThreads)
+    dequant_v8(const uint8_t* __restrict__ q, const float* __restrict__ scales, int64_t n32,
+               int64_t C, uint8_t* __restrict__ y) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n32; v += stride) {
+    const V8 c = ld_stream8(q + 32 * v);
+    const float s = scale_at<KIND>(scales, v * 32, C);
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 a = decode2<FMT>(c.w[i] & 0xFFFFu), b = decode2<FMT>(c.w[i] >> 16);
+      f[4 * i + 0] = __fmul_rn(a.x, s);
+      f[4 * i + 1] = __fmul_rn(a.y, s);
+      f[4 * i + 2] = __fmul_rn(b.x, s);
+      f[4 * i + 3] = __fmul_rn(b.y, s);
+    }
+    if constexpr (OUT == GS_F32) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        V8 o;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o.w[j] = __float_as_uint(f[8 * k + j]);
+        st_stream8(y + 128 * v + 32 * k, o);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        V8 o;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o.w[j] = cvt_f32x2_bf16x2(f[16 * k + 2 * j + 1], f[16 * k + 2 * j]);
+        st_stream8(y + 64 * v + 32 * k, o);
+      }
+    }
+  }
+}
+
 // Element-wise path for any alignment and for the ragged tail.
 template <int KIND, int FMT, int OUT>
 __global__ void __launch_bounds__(kDeqThreads)
@@ -88,8 +127,19 @@ static cudaError_t dequant_t(const uint8_t* q, const float* scales, int64_t R, i
   const int64_t cap = (int64_t)sm_count() * 8;
   const size_t ysz = OUT == GS_F32 ? 4 : 2;
   const bool vec = ((uintptr_t)q & 15u) == 0 && ((uintptr_t)y & 15u) == 0;
+  const bool vec8 = ((uintptr_t)q & 31u) == 0 && ((uintptr_t)y & 31u) == 0;
   int64_t done = 0;
-  if (vec && n >= 16) {
+  if (vec8 && n >= 32) {
+    const int64_t n32 = n / 32;
+    int64_t grid = (n32 + kDeqThreads - 1) / kDeqThreads;
+    const int64_t cap8 = (int64_t)sm_count() * 32;
+    if (grid > cap8) grid = cap8;
+    dequant_v8<KIND, FMT, OUT><<<(unsigned)grid, kDeqThreads, 0, st>>>(
+        q, scales, n32, C, reinterpret_cast<uint8_t*>(y));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    done = n32 * 32;
+  } else if (vec && n >= 16) {
     const int64_t n16 = n / 16;
     int64_t grid = (n16 + kDeqThreads - 1) / kDeqThreads;
     if (grid > cap) grid = cap;

@@ -101,6 +101,66 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
+// ---- 1x128, 16-bit input, 32-byte vectors: one 8-lane group per tile -------
+// Each lane loads 16 elements (32 B); the 8 lanes of a group reduce the tile
+// amax with three shuffles and write 16 codes each (one 16-byte store), so a
+// warp moves four tiles per slot and keeps two slots in flight.
+constexpr int kQ8Unroll = 2;
+
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+template <typename Tag, int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_1x128_v8(const uint8_t* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ q,
+                   float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t n_slots = (n_tiles + 3) >> 2;
+  // uniform loop bound across the warp: every lane reaches the shuffles
+  for (int64_t p0 = warp; p0 < n_slots; p0 += n_warps * kQ8Unroll) {
+    V8 v[kQ8Unroll];
+#pragma unroll
+    for (int u = 0; u < kQ8Unroll; ++u) {
+      const int64_t t = 4 * (p0 + u * n_warps) + grp;
+      if (t < n_tiles) v[u] = ld_stream8(x + t * 256 + l8 * 32);
+      else
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[u].w[j] = 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kQ8Unroll; ++u) {
+      const int64_t t = 4 * (p0 + u * n_warps) + grp;
+      const uint32_t mm = 0x7FFF7FFFu;
+      uint32_t m = __vmaxu2(__vmaxu2(__vmaxu2(v[u].w[0] & mm, v[u].w[1] & mm),
+                                     __vmaxu2(v[u].w[2] & mm, v[u].w[3] & mm)),
+                            __vmaxu2(__vmaxu2(v[u].w[4] & mm, v[u].w[5] & mm),
+                                     __vmaxu2(v[u].w[6] & mm, v[u].w[7] & mm)));
+      m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
+      const bool fin = isfinite(s);
+      const float r = __frcp_rn(s);
+      uint32_t c[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        c[j] = quant_pair<FMT>(hi16<Tag>(v[u].w[2 * j]), lo16<Tag>(v[u].w[2 * j]), s, r, fin) |
+               (quant_pair<FMT>(hi16<Tag>(v[u].w[2 * j + 1]), lo16<Tag>(v[u].w[2 * j + 1]), s, r,
+                                fin)
+                << 16);
+      if (t < n_tiles) {
+        st_stream16(q + t * 128 + l8 * 16, make_uint4(c[0], c[1], c[2], c[3]));
+        if (l8 == 0) scales[t] = s;
+      }
+    }
+  }
+}
+
 // ---- 1x128, FP32 input, vectorised: one warp per tile ------------------------
 template <int FMT>
 __global__ void __launch_bounds__(kQuantThreads)
@@ -314,6 +374,19 @@ static cudaError_t quant_1x128_t(const void* x, int64_t R, int64_t C, uint8_t* q
   const int64_t n_tiles = R * (C / 128);
   const uintptr_t xa = (uintptr_t)x, qa = (uintptr_t)q;
   if constexpr (DT != GS_F32) {
+    if ((xa & 31u) == 0 && (qa & 15u) == 0) {
+      using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
+      auto k = quant_1x128_v8<Tag, FMT>;
+      // oversubscribed grid: 16 CTAs per SM, each pass of a CTA moves 64 tiles
+      int64_t grid = (int64_t)sm_count() * 16;
+      const int64_t need = (n_tiles + 4 * (kQuantThreads / 32) * kQ8Unroll - 1) /
+                           (4 * (kQuantThreads / 32) * kQ8Unroll);
+      if (grid > need) grid = need;
+      if (grid < 1) grid = 1;
+      k<<<(unsigned)grid, kQuantThreads, 0, st>>>(reinterpret_cast<const uint8_t*>(x), n_tiles, q,
+                                                  scales);
+      return cudaGetLastError();
+    }
     if ((xa & 15u) == 0 && (qa & 7u) == 0) {
       using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
       auto k = quant_1x128_v16<Tag, FMT>;

@@ -145,6 +145,26 @@ __device__ __forceinline__ uint32_t quant_pair(float hi, float lo, float s, floa
 }
 
 // ---- streaming memory access ----------------------------------------------
+// 32-byte (256-bit) global accesses, new with sm_100: half the memory
+// instructions of 16-byte accesses for the same bytes in flight.
+struct V8 {
+  uint32_t w[8];
+};
+__device__ __forceinline__ V8 ld_stream8(const void* p) {
+  V8 a;
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(a.w[0]), "=r"(a.w[1]), "=r"(a.w[2]), "=r"(a.w[3]), "=r"(a.w[4]),
+                 "=r"(a.w[5]), "=r"(a.w[6]), "=r"(a.w[7])
+               : "l"(p));
+  return a;
+}
+__device__ __forceinline__ void st_stream8(void* p, const V8& a) {
+  asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+               "r"(a.w[0]), "r"(a.w[1]), "r"(a.w[2]), "r"(a.w[3]), "r"(a.w[4]), "r"(a.w[5]),
+               "r"(a.w[6]), "r"(a.w[7])
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -9,13 +9,15 @@ namespace gs {
 
 // One contiguous run of a gradient tensor: at most kChunkElems elements.
 // Chunk starts are multiples of kChunkElems from the tensor's start, so
-// every chunk of a tensor keeps the tensor's alignment.
+// every chunk of a tensor keeps the tensor's alignment.  A full chunk is
+// exactly one pass of a 256-thread CTA moving two 32-byte vectors (16 FP16
+// values each) per thread.
 struct Chunk {
   const uint16_t* in;  // scaled FP16 gradients
   float* out;          // FP32 unscaled output
   int64_t n;
 };
-constexpr int64_t kChunkElems = 32768;
+constexpr int64_t kChunkElems = 8192;
 
 // Per-list device workspace of the last-CTA epilogue.  Both words return
 // to zero at the end of every call.

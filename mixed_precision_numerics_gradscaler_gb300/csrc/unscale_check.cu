@@ -8,10 +8,13 @@
 //   found_inf = any scaled FP16 input with an all-ones exponent field,
 //   then S / growth tracker updated on the device by the last CTA to finish.
 //
-// Layout: a persistent grid walks the list's chunk table (32 Ki-element
-// chunks, grid-stride).  Each thread moves 16-byte vectors: 8 FP16 in, 2 x 4
-// FP32 out, several vectors in flight per thread.  HBM-bound: 6 bytes per
-// element (2 read + 4 written).
+// Layout: an oversubscribed grid (32 CTAs per SM, four or more waves of
+// resident CTAs) walks the list's chunk table grid-stride.  A full 8192-
+// element chunk is one pass of a 256-thread CTA: each thread issues two
+// 32-byte loads (16 FP16 each) and four 32-byte stores (8 FP32 each).
+// Chunks that are short or not 32-byte aligned take a 16-byte path with a
+// scalar head and tail.  HBM-bound: 6 bytes per element (2 read + 4
+// written).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -23,6 +26,8 @@ namespace gs {
 
 constexpr int kUnscaleThreads = 256;
 constexpr int kUnscaleUnroll = 4;
+constexpr int kUnscaleCtasPerSm = 32;
+static_assert(kChunkElems == 2 * 16 * kUnscaleThreads, "one pass of v8 pairs per chunk");
 
 // 0xFFFF in each 16-bit lane whose exponent field is all ones (Inf / NaN).
 __device__ __forceinline__ uint32_t nonfinite2(uint32_t w) {
@@ -49,6 +54,34 @@ __device__ __forceinline__ void unscale1(const uint16_t* in, float* out, int64_t
   const uint32_t h = in[i];
   bad |= ((h & 0x7C00u) == 0x7C00u);
   out[i] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), inv);
+}
+
+// 16 FP16 -> 16 FP32 (two 32-byte stores).
+__device__ __forceinline__ void unscale16(const V8& v, float inv, uint8_t* out, uint32_t& bad) {
+  V8 a, b;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    bad |= nonfinite2(v.w[j]) | nonfinite2(v.w[j + 4]);
+    a.w[2 * j] = __float_as_uint(__fmul_rn(lo_f16(v.w[j]), inv));
+    a.w[2 * j + 1] = __float_as_uint(__fmul_rn(hi_f16(v.w[j]), inv));
+    b.w[2 * j] = __float_as_uint(__fmul_rn(lo_f16(v.w[j + 4]), inv));
+    b.w[2 * j + 1] = __float_as_uint(__fmul_rn(hi_f16(v.w[j + 4]), inv));
+  }
+  st_stream8(out, a);
+  st_stream8(out + 32, b);
+}
+
+// Full, 32-byte-aligned chunk: two loads in flight per thread, then stores.
+__device__ __forceinline__ uint32_t unscale_chunk_full(const Chunk ch, float inv) {
+  const uint8_t* in = reinterpret_cast<const uint8_t*>(ch.in);
+  uint8_t* out = reinterpret_cast<uint8_t*>(ch.out);
+  const int v0 = threadIdx.x, v1 = threadIdx.x + kUnscaleThreads;
+  const V8 a = ld_stream8(in + 32 * v0);
+  const V8 b = ld_stream8(in + 32 * v1);
+  uint32_t bad = 0;
+  unscale16(a, inv, out + 64 * v0, bad);
+  unscale16(b, inv, out + 64 * v1, bad);
+  return bad;
 }
 
 __device__ __forceinline__ uint32_t unscale_chunk(const Chunk ch, float inv) {
@@ -87,7 +120,11 @@ __global__ void __launch_bounds__(kUnscaleThreads)
   const float S = *scale;
   const float inv = (float)(1.0 / (double)S);
   uint32_t bad = 0;
-  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) bad |= unscale_chunk(chunks[c], inv);
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    const Chunk ch = chunks[c];
+    const bool full = ch.n == kChunkElems && ((((uintptr_t)ch.in) | ((uintptr_t)ch.out)) & 31u) == 0;
+    bad |= full ? unscale_chunk_full(ch, inv) : unscale_chunk(ch, inv);
+  }
 
   const int any_bad = __syncthreads_or(bad != 0);
   if (threadIdx.x != 0) return;
@@ -122,14 +159,7 @@ cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks,
                                         float* scale, int32_t* tracker, int32_t* found,
                                         int64_t* skipped, float growth, float backoff,
                                         int32_t interval, cudaStream_t stream) {
-  static int occ = 0;  // resident CTAs per SM (same on every GB300)
-  if (occ == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, unscale_check_update_kernel, kUnscaleThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-  }
-  int64_t grid = (int64_t)sm_count() * occ;
+  int64_t grid = (int64_t)sm_count() * kUnscaleCtasPerSm;
   if (grid > n_chunks) grid = n_chunks;
   if (grid < 1) grid = 1;
   unscale_check_update_kernel<<<(unsigned)grid, kUnscaleThreads, 0, stream>>>(

@@ -86,7 +86,7 @@ def test_quant_128x128_shapes(gs, orc, fmt, dt, R, C):
 
 
 @pytest.mark.parametrize("br", [1, 128])
-@pytest.mark.parametrize("x_off,q_off", [(1, 0), (0, 1), (3, 5)])
+@pytest.mark.parametrize("x_off,q_off", [(1, 0), (0, 1), (3, 5), (8, 8), (8, 0), (16, 8)])
 def test_quant_misaligned_buffers(gs, orc, br, x_off, q_off):
     rng = np.random.default_rng(x_off + 10 * q_off + br)
     R, C = 256, 384
@@ -95,6 +95,28 @@ def test_quant_misaligned_buffers(gs, orc, br, x_off, q_off):
     xd = base[x_off:x_off + R * C].view(R, C)
     xd.copy_(to_dev16(xh, torch.bfloat16).view(R, C))
     _check_block(gs, orc, xh, xd, "bf16", br, 128, "e4m3", q_off=q_off)
+
+
+@pytest.mark.parametrize("y_off", [1, 4, 8, 16])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_dequant_misaligned_output(gs, orc, y_off, out):
+    rng = np.random.default_rng(y_off)
+    R, C = 130, 256
+    xh, xd = _host_input(rng, R, C, "bf16")
+    q = torch.empty(R, C, dtype=torch.uint8, device=DEV)
+    s = torch.empty(R, C // 128, dtype=torch.float32, device=DEV)
+    gs.fp8_quant_block(xd, 1, 128, "e4m3", q, s)
+    base = torch.zeros(R * C + 32, dtype=TDT[out], device=DEV)
+    y = base[y_off:y_off + R * C].view(R, C)
+    gs.fp8_dequant(q, s, 1, 128, "e4m3", y)
+    rq, rs = orc.quant_block(xh, 1, 128, 0, dtype=1)
+    ry = orc.dequant(rq, rs, 1, 128, 0, out_dtype=ODT[out])
+    torch.cuda.synchronize()
+    if out == "f32":
+        assert_same_f32(y.cpu().numpy(), ry, "dequant misaligned")
+    else:
+        assert same_bf16(bits_of(y), ry).all()
+    assert (base[:y_off] == 0).all() and (base[y_off + R * C:] == 0).all()
 
 
 def test_cfg1_activation_quant(gs, orc):

@@ -126,13 +126,13 @@ def test_empty_list_counts_a_clean_step(gs):
     tl.close()
 
 
-@pytest.mark.parametrize("in_off,out_off", [(1, 0), (0, 1), (1, 1), (3, 2), (5, 5)])
+@pytest.mark.parametrize("in_off,out_off", [(1, 0), (0, 1), (1, 1), (3, 2), (5, 5), (8, 4), (16, 8), (8, 8)])
 def test_misaligned_views(gs, orc, in_off, out_off):
     rng = np.random.default_rng(in_off * 10 + out_off)
     n = 70001
     h = (rng.standard_normal(n) * 50).astype(np.float16).view(np.uint16)
-    base_in = torch.zeros(n + 8, dtype=torch.float16, device=DEV)
-    base_out = torch.zeros(n + 8, dtype=torch.float32, device=DEV)
+    base_in = torch.zeros(n + 32, dtype=torch.float16, device=DEV)
+    base_out = torch.zeros(n + 32, dtype=torch.float32, device=DEV)
     gin = base_in[in_off:in_off + n]
     gin.copy_(to_dev16(h, torch.float16))
     gout = base_out[out_off:out_off + n]
