@@ -131,6 +131,36 @@ int gs_scaler_state_get(const float* scale, const int32_t* growth_tracker, float
 int gs_scaler_state_set(float* scale, int32_t* growth_tracker, float h_scale,
                         int32_t h_growth_tracker, void* stream);
 
+/* Allocation-free form of gs_unscale_check_update.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory (code running inside an allocator's own callbacks, or in a
+ * process whose device memory another runtime has reserved up front), and so
+ * cannot call gs_tensor_list_create.
+ *   grads / outs / numels / n_tensors -- as for gs_tensor_list_create, given
+ *       on every call (nothing is captured); the remaining arguments and the
+ *       results are exactly those of gs_unscale_check_update.
+ * The chunk table and the epilogue words live in one fixed device array of
+ * this library (768 KiB + 256 B per GPU that loads the library, held until
+ * the process exits).  Limits: at most 960 tensors and 32768 chunks of 8192
+ * elements (268,435,456 elements in total); larger lists return
+ * GS_ERR_SHAPE before anything is launched (see gs_noalloc_limits).
+ * The call makes no cudaMalloc / cudaFree and allocates nothing.  Its first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current): make that first call before any stream capture.
+ * Every call shares the one array and its contents persist between calls; the
+ * call clears what must start at zero itself.  Calls that overlap on the GPU
+ * (on different streams, or from different host threads without ordering)
+ * race on the array: order them on one stream. */
+int gs_unscale_check_update_noalloc(const void* const* grads, void* const* outs,
+                                    const int64_t* numels, int32_t n_tensors, float* scale,
+                                    int32_t* growth_tracker, int32_t* found_inf, int64_t* skipped,
+                                    float growth_factor, float backoff_factor,
+                                    int32_t growth_interval, void* stream);
+
+/* The limits of gs_unscale_check_update_noalloc (host values; any pointer
+ * may be NULL). */
+int gs_noalloc_limits(int32_t* max_tensors, int64_t* max_chunks, int64_t* chunk_elems);
+
 /* ------------------------------------------------------------------------
  * FP8 quantisation with fine-grained scaling ([P5] "FP8 training", the
  * fp8_scaling.py listing: per-block amax, clamp at 1e-12, divide by MAX;

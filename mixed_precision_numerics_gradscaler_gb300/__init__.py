@@ -20,6 +20,7 @@ __all__ = [
     "gs_status_str", "gs_version", "gs_tensor_list_create", "gs_unscale_check_update",
     "gs_scaler_state_get", "gs_scaler_state_set", "fp8_quant_block", "fp8_quant_tensor",
     "fp8_dequant", "gs_ws_bytes", "gs_device_status", "lib_path",
+    "gs_unscale_check_update_noalloc", "gs_noalloc_limits",
 ]
 
 GS_OK, GS_ERR_NULL, GS_ERR_SHAPE, GS_ERR_DTYPE, GS_ERR_ARG, GS_ERR_CUDA, GS_ERR_TIMEOUT = range(7)
@@ -58,6 +59,8 @@ def _load_lib() -> ctypes.CDLL:
         "fp8_quant_tensor": (ci, [vp, ci, i64, ci, vp, vp, vp, vp]),
         "fp8_dequant": (ci, [vp, vp, i64, i64, i32, i32, ci, ci, vp, vp]),
         "gs_device_status": (ci, [ctypes.POINTER(i32), vp]),
+        "gs_unscale_check_update_noalloc": (ci, [vp, vp, vp, i32, vp, vp, vp, vp, f32, f32, i32, vp]),
+        "gs_noalloc_limits": (ci, [ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -162,6 +165,39 @@ def gs_unscale_check_update(tlist: TensorList, scale: torch.Tensor, growth_track
                                         _ptr(found_inf), _ptr(skipped), growth_factor,
                                         backoff_factor, growth_interval, _stream(stream)),
            "gs_unscale_check_update")
+
+
+def gs_unscale_check_update_noalloc(grads: list[torch.Tensor], outs: list[torch.Tensor],
+                                    scale: torch.Tensor, growth_tracker: torch.Tensor,
+                                    found_inf: torch.Tensor, skipped: torch.Tensor | None = None,
+                                    growth_factor: float = 2.0, backoff_factor: float = 0.5,
+                                    growth_interval: int = 2000, stream=None) -> None:
+    """The GradScaler step without any device allocation (for callers that
+    cannot allocate): same results as gs_unscale_check_update, the list
+    given on every call, the chunk table kept in the library's fixed device
+    array."""
+    if len(grads) != len(outs):
+        raise ValueError("grads and outs differ in length")
+    for g, o in zip(grads, outs):
+        _contig(g, "grad")
+        _contig(o, "out")
+        if g.dtype != torch.float16 or o.dtype != torch.float32 or g.numel() != o.numel():
+            raise ValueError("each grad must be float16 and its out float32 of equal numel")
+    n = len(grads)
+    gp = (ctypes.c_void_p * max(n, 1))(*[g.data_ptr() for g in grads])
+    op = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in outs])
+    ne = (ctypes.c_int64 * max(n, 1))(*[g.numel() for g in grads])
+    _check(_lib.gs_unscale_check_update_noalloc(gp, op, ne, n, _ptr(scale), _ptr(growth_tracker),
+                                                _ptr(found_inf), _ptr(skipped), growth_factor,
+                                                backoff_factor, growth_interval, _stream(stream)),
+           "gs_unscale_check_update_noalloc")
+
+
+def gs_noalloc_limits() -> tuple[int, int, int]:
+    t, c, e = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64()
+    _check(_lib.gs_noalloc_limits(ctypes.byref(t), ctypes.byref(c), ctypes.byref(e)),
+           "gs_noalloc_limits")
+    return t.value, c.value, e.value
 
 
 def gs_scaler_state_get(scale: torch.Tensor, growth_tracker: torch.Tensor,

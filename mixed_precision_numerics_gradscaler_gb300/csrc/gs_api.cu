@@ -47,6 +47,8 @@ int sm_count() {
   return cache[d];
 }
 
+void record_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }
+
 static int32_t* device_status_ptr() {
   static int32_t* cache[kMaxDevices] = {nullptr};
   static std::mutex mu;

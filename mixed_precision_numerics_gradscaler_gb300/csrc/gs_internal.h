@@ -31,6 +31,9 @@ struct ListWs {
 int sm_count();
 int current_device();
 
+// Records e as the calling thread's last CUDA error (gs_last_cuda_error).
+void record_cuda_error(cudaError_t e);
+
 // Launchers.  Each returns the launch's cudaError_t.
 cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks, ListWs* ws,
                                         float* scale, int32_t* tracker, int32_t* found,

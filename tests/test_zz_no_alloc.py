@@ -1,0 +1,88 @@
+"""The allocation-free GradScaler step, gs_unscale_check_update_noalloc.
+
+It serves callers that cannot allocate device memory -- code running inside
+an allocator's own callbacks, or a process whose device memory another
+runtime has reserved up front -- and therefore cannot build the chunk table
+that gs_tensor_list_create allocates.  Its results must equal those of
+gs_unscale_check_update on the same inputs, call after call.
+
+The file name makes pytest collect it after every other test file."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import datagen as dg
+from datagen import workloads as wl
+from gpu_helpers import DEV, assert_same_f32, to_dev16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gs():
+    import mixed_precision_numerics_gradscaler_gb300 as gs
+    torch.cuda.set_device(0)
+    return gs
+
+
+def _state(scale):
+    return (torch.tensor([scale], dtype=torch.float32, device=DEV),
+            torch.zeros(1, dtype=torch.int32, device=DEV),
+            torch.zeros(1, dtype=torch.int32, device=DEV),
+            torch.zeros(1, dtype=torch.int64, device=DEV))
+
+
+def test_noalloc_matches_list_entry_point_on_two_calls_in_a_row(gs):
+    cfg = wl.cfg1_grads()                      # 8 tensors, 2^20 elements, odd sizes
+    grads = [torch.empty(n, dtype=torch.float16, device=DEV) for n in cfg.numels]
+    outs_ref = [torch.empty(n, dtype=torch.float32, device=DEV) for n in cfg.numels]
+    outs_new = [torch.full((n,), 123.0, dtype=torch.float32, device=DEV) for n in cfg.numels]
+    tl = gs.gs_tensor_list_create(grads, outs_ref)
+    ref, new = _state(cfg.init_scale), _state(cfg.init_scale)
+    for call, step in enumerate([4, 5]):       # step 5 carries the planted +Inf
+        hosts = [dg.fill_host(cfg.spec(t, step), 0, n) for t, n in enumerate(cfg.numels)]
+        p = cfg.plant(step)
+        if p is not None:
+            hosts[p[0]][p[1]] = cfg.plant_bits
+        for g, h in zip(grads, hosts):
+            g.copy_(to_dev16(h, torch.float16))
+        gs.gs_unscale_check_update(tl, *ref, 2.0, 0.5, cfg.growth_interval)
+        gs.gs_unscale_check_update_noalloc(grads, outs_new, *new, 2.0, 0.5, cfg.growth_interval)
+        torch.cuda.synchronize()
+        for t, (a, b) in enumerate(zip(outs_new, outs_ref)):
+            assert_same_f32(a.cpu().numpy(), b.cpu().numpy(), f"call {call} tensor {t}")
+        for a, b in zip(new, ref):
+            assert a.item() == b.item(), f"call {call}: scaler state differs"
+        assert int(new[2].item()) == (1 if p is not None else 0)
+    tl.close()
+
+
+def test_noalloc_rejects_lists_beyond_its_fixed_array(gs):
+    max_tensors, max_chunks, chunk_elems = gs.gs_noalloc_limits()
+    assert max_chunks * chunk_elems == 268435456
+    scale, tracker, found, skipped = _state(8.0)
+    g = torch.zeros(16, dtype=torch.float16, device=DEV)
+    o = torch.zeros(16, dtype=torch.float32, device=DEV)
+    lib = gs._lib
+
+    def call(n_tensors, numel):
+        k = max(n_tensors, 1)
+        gp = (ctypes.c_void_p * k)(*([g.data_ptr()] * k))
+        op = (ctypes.c_void_p * k)(*([o.data_ptr()] * k))
+        ne = (ctypes.c_int64 * k)(*([numel] * k))
+        return lib.gs_unscale_check_update_noalloc(
+            gp, op, ne, n_tensors, scale.data_ptr(), tracker.data_ptr(), found.data_ptr(),
+            skipped.data_ptr(), 2.0, 0.5, 10, torch.cuda.current_stream().cuda_stream)
+
+    # more tensors than the table holds, more elements than the array holds:
+    # rejected on the host, before anything is launched or read
+    assert call(max_tensors + 1, 16) == gs.GS_ERR_SHAPE
+    assert call(1, max_chunks * chunk_elems + 1) == gs.GS_ERR_SHAPE
+    torch.cuda.synchronize()
+    assert scale.item() == 8.0 and tracker.item() == 0 and found.item() == 0
+    # a list within the limits goes through and counts a clean step
+    assert call(1, 16) == gs.GS_OK
+    torch.cuda.synchronize()
+    assert tracker.item() == 1
