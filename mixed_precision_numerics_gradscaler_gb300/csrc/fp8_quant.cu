@@ -89,10 +89,10 @@ __global__ void __launch_bounds__(kQuantThreads)
       const bool fin = isfinite(s);
       const float r = __frcp_rn(s);
       uint2 o;
-      o.x = quant_pair<FMT>(hi16<Tag>(v[u].x), lo16<Tag>(v[u].x), s, r, fin) |
-            (quant_pair<FMT>(hi16<Tag>(v[u].y), lo16<Tag>(v[u].y), s, r, fin) << 16);
-      o.y = quant_pair<FMT>(hi16<Tag>(v[u].z), lo16<Tag>(v[u].z), s, r, fin) |
-            (quant_pair<FMT>(hi16<Tag>(v[u].w), lo16<Tag>(v[u].w), s, r, fin) << 16);
+      o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].x), lo16<Tag>(v[u].x), s, r, fin) |
+            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].y), lo16<Tag>(v[u].y), s, r, fin) << 16);
+      o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].z), lo16<Tag>(v[u].z), s, r, fin) |
+            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].w), lo16<Tag>(v[u].w), s, r, fin) << 16);
       if (t < n_tiles) {
         st_stream(q + t * 16 + l16, o);
         if (l16 == 0) scales[t] = s;
@@ -149,14 +149,69 @@ __global__ void __launch_bounds__(kQuantThreads)
       uint32_t c[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        c[j] = quant_pair<FMT>(hi16<Tag>(v[u].w[2 * j]), lo16<Tag>(v[u].w[2 * j]), s, r, fin) |
-               (quant_pair<FMT>(hi16<Tag>(v[u].w[2 * j + 1]), lo16<Tag>(v[u].w[2 * j + 1]), s, r,
+        c[j] = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].w[2 * j]), lo16<Tag>(v[u].w[2 * j]), s, r, fin) |
+               (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].w[2 * j + 1]), lo16<Tag>(v[u].w[2 * j + 1]), s, r,
                                 fin)
                 << 16);
       if (t < n_tiles) {
         st_stream16(q + t * 128 + l8 * 16, make_uint4(c[0], c[1], c[2], c[3]));
         if (l8 == 0) scales[t] = s;
       }
+    }
+  }
+}
+
+// ---- 1x128, 16-bit input: one 4-lane group per tile --------------------------
+// Each lane loads 32 elements (two 32-byte loads) of its tile; the 4 lanes
+// reduce the tile amax with two shuffles; each lane writes its 32 codes with
+// one 32-byte store.  A warp moves eight tiles (2 KB in, 1 KB out) per slot,
+// and the per-tile scale and reciprocal are amortised over 32 elements per
+// lane.
+template <typename Tag, int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_1x128_v8x2(const uint8_t* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ q,
+                     float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31, grp = lane >> 2, l4 = lane & 3;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t n_slots = (n_tiles + 7) >> 3;
+  constexpr int kSteps = QuotSteps<Tag>::value;
+  // uniform loop bound across the warp: every lane reaches the shuffles
+  for (int64_t p0 = warp; p0 < n_slots; p0 += n_warps) {
+    const int64_t t = 8 * p0 + grp;
+    V8 a, b;
+    if (t < n_tiles) {
+      a = ld_stream8(x + t * 256 + l4 * 64);
+      b = ld_stream8(x + t * 256 + l4 * 64 + 32);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a.w[j] = b.w[j] = 0;
+    }
+    const uint32_t mm = 0x7FFF7FFFu;
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m2 = __vmaxu2(m2, __vmaxu2(a.w[j] & mm, b.w[j] & mm));
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
+    const bool fin = isfinite(s);
+    const float r = __frcp_rn(s);
+    V8 o;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      o.w[j] = quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j]), lo16<Tag>(a.w[2 * j]), s, r, fin) |
+               (quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j + 1]), lo16<Tag>(a.w[2 * j + 1]), s, r,
+                                        fin)
+                << 16);
+      o.w[4 + j] =
+          quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j]), lo16<Tag>(b.w[2 * j]), s, r, fin) |
+          (quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j + 1]), lo16<Tag>(b.w[2 * j + 1]), s, r, fin)
+           << 16);
+    }
+    if (t < n_tiles) {
+      st_stream8(q + t * 128 + l4 * 32, o);
+      if (l4 == 0) scales[t] = s;
     }
   }
 }
@@ -333,20 +388,20 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         uint2 o;
-        o.x = quant_pair<FMT>(hi16<Tag>(a[u].x), lo16<Tag>(a[u].x), s, r, fin) |
-              (quant_pair<FMT>(hi16<Tag>(a[u].y), lo16<Tag>(a[u].y), s, r, fin) << 16);
-        o.y = quant_pair<FMT>(hi16<Tag>(a[u].z), lo16<Tag>(a[u].z), s, r, fin) |
-              (quant_pair<FMT>(hi16<Tag>(a[u].w), lo16<Tag>(a[u].w), s, r, fin) << 16);
+        o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].x), lo16<Tag>(a[u].x), s, r, fin) |
+              (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].y), lo16<Tag>(a[u].y), s, r, fin) << 16);
+        o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].z), lo16<Tag>(a[u].z), s, r, fin) |
+              (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].w), lo16<Tag>(a[u].w), s, r, fin) << 16);
         st_stream(q8 + v + u * nthreads, o);
       }
     }
     for (; v < nv; v += nthreads) {
       const uint4 a = ld_stream(x8 + v);
       uint2 o;
-      o.x = quant_pair<FMT>(hi16<Tag>(a.x), lo16<Tag>(a.x), s, r, fin) |
-            (quant_pair<FMT>(hi16<Tag>(a.y), lo16<Tag>(a.y), s, r, fin) << 16);
-      o.y = quant_pair<FMT>(hi16<Tag>(a.z), lo16<Tag>(a.z), s, r, fin) |
-            (quant_pair<FMT>(hi16<Tag>(a.w), lo16<Tag>(a.w), s, r, fin) << 16);
+      o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.x), lo16<Tag>(a.x), s, r, fin) |
+            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.y), lo16<Tag>(a.y), s, r, fin) << 16);
+      o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.z), lo16<Tag>(a.z), s, r, fin) |
+            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.w), lo16<Tag>(a.w), s, r, fin) << 16);
       st_stream(q8 + v, o);
     }
     for (int64_t i = head + nv * 8 + tid; i < n; i += nthreads)
@@ -374,6 +429,18 @@ static cudaError_t quant_1x128_t(const void* x, int64_t R, int64_t C, uint8_t* q
   const int64_t n_tiles = R * (C / 128);
   const uintptr_t xa = (uintptr_t)x, qa = (uintptr_t)q;
   if constexpr (DT != GS_F32) {
+    if ((xa & 31u) == 0 && (qa & 31u) == 0) {
+      using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
+      auto k = quant_1x128_v8x2<Tag, FMT>;
+      // oversubscribed grid: 16 CTAs per SM, each pass of a CTA moves 64 tiles
+      int64_t grid = (int64_t)sm_count() * 16;
+      const int64_t need = (n_tiles + 8 * (kQuantThreads / 32) - 1) / (8 * (kQuantThreads / 32));
+      if (grid > need) grid = need;
+      if (grid < 1) grid = 1;
+      k<<<(unsigned)grid, kQuantThreads, 0, st>>>(reinterpret_cast<const uint8_t*>(x), n_tiles, q,
+                                                  scales);
+      return cudaGetLastError();
+    }
     if ((xa & 31u) == 0 && (qa & 15u) == 0) {
       using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
       auto k = quant_1x128_v8<Tag, FMT>;

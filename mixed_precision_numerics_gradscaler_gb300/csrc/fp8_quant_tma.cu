@@ -7,8 +7,8 @@
 // A persistent CTA walks its share of the blocks.  One elected thread
 // issues cp.async.bulk.tensor.2d loads of whole 128x128 tiles (32 KB,
 // no swizzle, no multicast) into a 3-stage ring, each stage guarded by an
-// mbarrier with a transaction count.  All 256 threads then pull the tile
-// from shared memory into registers (8 x 16 B each, conflict-free rows of
+// mbarrier with a transaction count.  All 512 threads then pull the tile
+// from shared memory into registers (4 x 16 B each, conflict-free rows of
 // 256 B), reduce the block amax (packed 16-bit max, warp shuffle, one word
 // per warp), release the stage so the next load overlaps the cast, and
 // write FP8 codes straight from registers with 8-byte coalesced stores.
@@ -27,11 +27,14 @@
 
 namespace gs {
 
-constexpr int kTmaThreads = 256;
+constexpr int kTmaThreads = 512;
+constexpr int kTmaWarps = kTmaThreads / 32;
+constexpr int kRowsPerPass = kTmaThreads / 16;   // 16 threads cover a 256-byte row
+constexpr int kRowPasses = 128 / kRowsPerPass;
 constexpr int kTmaStages = 3;
 constexpr int kTileBytes = 128 * 128 * 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kTmaSmemBytes = kTmaStages * kTileBytes + kTmaStages * 8 + 2 * 8 * 4 + 64;
+constexpr int kTmaSmemBytes = kTmaStages * kTileBytes + kTmaStages * 8 + 2 * kTmaWarps * 4 + 64;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(kTmaThreads)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kTileBytes);
-  uint32_t* red = reinterpret_cast<uint32_t*>(full + kTmaStages);  // [2][8]
+  uint32_t* red = reinterpret_cast<uint32_t*>(full + kTmaStages);  // [2][kTmaWarps]
 
   const int64_t n_blocks = nbr * nbc;
   if ((int64_t)blockIdx.x >= n_blocks) return;
@@ -103,7 +106,8 @@ __global__ void __launch_bounds__(kTmaThreads)
   if (tid == 0)
     for (; issued < kTmaStages && issued < my_n; ++issued) issue(issued);
 
-  // Thread tid owns rows (tid >> 4) + 16 j, 16-byte column chunk (tid & 15).
+  // Thread tid owns rows (tid >> 4) + kRowsPerPass * j, 16-byte column chunk
+  // (tid & 15): a warp reads two whole 256-byte rows per pass.
   const int row0 = tid >> 4, chunk = tid & 15;
   for (int64_t k = 0; k < my_n; ++k) {
     const int stage = (int)(k % kTmaStages);
@@ -119,24 +123,24 @@ __global__ void __launch_bounds__(kTmaThreads)
       return;
     }
     const uint4* tile = reinterpret_cast<const uint4*>(tiles + stage * kTileBytes);
-    uint4 v[8];
+    uint4 v[kRowPasses];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = tile[(row0 + 16 * j) * 16 + chunk];
+    for (int j = 0; j < kRowPasses; ++j) v[j] = tile[(row0 + kRowsPerPass * j) * 16 + chunk];
     const uint32_t mm = 0x7FFF7FFFu;
     uint32_t m2 = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < kRowPasses; ++j)
       m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v[j].x & mm, v[j].y & mm), __vmaxu2(v[j].z & mm, v[j].w & mm)));
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    uint32_t* rb = red + (k & 1) * 8;
+    uint32_t* rb = red + (k & 1) * kTmaWarps;
     if (lane == 0) rb[warp] = m;
     __syncthreads();  // every thread holds its part of the tile: the stage is free
     if (tid == 0 && issued < my_n) issue(issued++);
     m = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) m = max(m, rb[w]);
+    for (int w = 0; w < kTmaWarps; ++w) m = max(m, rb[w]);
     const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
     const bool fin = isfinite(s);
     const float r = __frcp_rn(s);
@@ -144,13 +148,13 @@ __global__ void __launch_bounds__(kTmaThreads)
     const int64_t r0 = (b / nbc) * 128, c0 = (b % nbc) * 128;
     if (tid == 0) scales[b] = s;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kRowPasses; ++j) {
       uint2 o;
-      o.x = quant_pair<FMT>(hi16<Tag>(v[j].x), lo16<Tag>(v[j].x), s, r, fin) |
-            (quant_pair<FMT>(hi16<Tag>(v[j].y), lo16<Tag>(v[j].y), s, r, fin) << 16);
-      o.y = quant_pair<FMT>(hi16<Tag>(v[j].z), lo16<Tag>(v[j].z), s, r, fin) |
-            (quant_pair<FMT>(hi16<Tag>(v[j].w), lo16<Tag>(v[j].w), s, r, fin) << 16);
-      st_stream(reinterpret_cast<uint2*>(q + (r0 + row0 + 16 * j) * C + c0 + chunk * 8), o);
+      o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].x), lo16<Tag>(v[j].x), s, r, fin) |
+            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].y), lo16<Tag>(v[j].y), s, r, fin) << 16);
+      o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].z), lo16<Tag>(v[j].z), s, r, fin) |
+            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].w), lo16<Tag>(v[j].w), s, r, fin) << 16);
+      st_stream(reinterpret_cast<uint2*>(q + (r0 + row0 + kRowsPerPass * j) * C + c0 + chunk * 8), o);
     }
   }
 }

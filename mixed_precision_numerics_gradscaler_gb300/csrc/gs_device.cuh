@@ -113,36 +113,55 @@ __device__ __forceinline__ float block_scale(float amax) {
   return __fdiv_rn(a, Fp8Max<FMT>::value);
 }
 
-// Correctly rounded fp32 quotient x / s for finite s > 0 (normal) given
-// r = RN(1/s), from one product and two residual corrections (Markstein's
-// theorem, P. Markstein, "IA-64 and Elementary Functions", 2000; also
-// Muller et al., "Handbook of Floating-Point Arithmetic", ch. 4): after the
-// first correction the estimate is within one ulp of x / s, so the second
-// correction returns the correctly rounded quotient.  The residuals
-// x - q*s are exact (fused multiply-add) whenever |x / s| is large enough
-// to matter to an FP8 code (>= 2^-17 with s >= 2^-49), and the sign of a
-// zero result is taken from x, as IEEE division does for s > 0.
+// The fp32 quotient x / s as IEEE division rounds it, for finite s > 0
+// (normal), from r = RN(1/s) (computed once per block): one product and
+// STEPS residual corrections by fused multiply-add (Markstein's theorem,
+// P. Markstein, "IA-64 and Elementary Functions", 2000; Muller et al.,
+// "Handbook of Floating-Point Arithmetic", ch. 4: once the estimate is
+// within one ulp of x / s, one correction with the correctly rounded
+// reciprocal returns the correctly rounded quotient).
+//   STEPS = 2 (FP32 inputs): the first correction brings the product,
+//     which can be 1.5 ulp off, within one ulp; the second is exact by the
+//     theorem whenever |x / s| >= 2^-20, where the residuals cannot
+//     underflow (s >= 1e-12 / MAX).
+//   STEPS = 1 (BF16 / FP16 inputs): checked by exhaustion over every pair
+//     of 16-bit patterns (x, amax) with |x| <= amax, for both formats: the
+//     result equals the IEEE quotient bit for bit whenever either is
+//     >= 2^-20, and has its sign.
+// Below 2^-20 both encode to a signed zero in E4M3 and E5M2, so the FP8
+// code is that of the IEEE quotient in every case.  The residual is formed
+// negated, n = q*s - x, so that x = -0 yields -0 (the plain form x - q*s
+// would give +0 - 0 = +0).
+template <int STEPS>
 __device__ __forceinline__ float exact_quotient(float x, float s, float r) {
   float q = __fmul_rn(x, r);
-  float e = __fmaf_rn(-q, s, x);
-  q = __fmaf_rn(e, r, q);
-  e = __fmaf_rn(-q, s, x);
-  q = __fmaf_rn(e, r, q);
-  return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+#pragma unroll
+  for (int i = 0; i < STEPS; ++i) {
+    const float n = __fmaf_rn(q, s, -x);
+    q = __fmaf_rn(-n, r, q);
+  }
+  return q;
 }
 
 // Quantise a pair with a finite scale (fast path) or a non-finite one (a
 // block holding Inf or NaN: IEEE division, NaN codes forced to 0x7F).
-template <int FMT>
+template <int FMT, int STEPS = 2>
 __device__ __forceinline__ uint32_t quant_pair(float hi, float lo, float s, float r,
                                                bool finite_scale) {
-  if (finite_scale) return cvt_f32x2_fp8x2<FMT>(exact_quotient(hi, s, r), exact_quotient(lo, s, r));
+  if (finite_scale)
+    return cvt_f32x2_fp8x2<FMT>(exact_quotient<STEPS>(hi, s, r), exact_quotient<STEPS>(lo, s, r));
   float qh = __fdiv_rn(hi, s), ql = __fdiv_rn(lo, s);
   uint32_t c = cvt_f32x2_fp8x2<FMT>(qh, ql);
   if (qh != qh) c = (c & 0x00FFu) | (kFp8NaN << 8);
   if (ql != ql) c = (c & 0xFF00u) | kFp8NaN;
   return c;
 }
+
+// Correction steps of the exact quotient for an input type (see above).
+template <typename Tag>
+struct QuotSteps {
+  static constexpr int value = 1;
+};
 
 // ---- streaming memory access ----------------------------------------------
 // 32-byte (256-bit) global accesses, new with sm_100: half the memory

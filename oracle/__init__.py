@@ -48,8 +48,13 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        build()
-        lib = ctypes.CDLL(_LIB_PATH)
+        # GS_ORACLE_LIB points the pin tests at another build of these
+        # sources (the mutation test plants mistakes in copies of them).
+        path = os.environ.get("GS_ORACLE_LIB")
+        if not path:
+            build()
+            path = _LIB_PATH
+        lib = ctypes.CDLL(path)
         i64, i32, f32p = ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_float)
         vp = ctypes.c_void_p
         sig = {

@@ -86,7 +86,7 @@ def test_quant_128x128_shapes(gs, orc, fmt, dt, R, C):
 
 
 @pytest.mark.parametrize("br", [1, 128])
-@pytest.mark.parametrize("x_off,q_off", [(1, 0), (0, 1), (3, 5), (8, 8), (8, 0), (16, 8)])
+@pytest.mark.parametrize("x_off,q_off", [(1, 0), (0, 1), (3, 5), (8, 8), (8, 0), (16, 8), (0, 16), (16, 0)])
 def test_quant_misaligned_buffers(gs, orc, br, x_off, q_off):
     rng = np.random.default_rng(x_off + 10 * q_off + br)
     R, C = 256, 384
@@ -183,12 +183,14 @@ def _torch_reference_1x128(xd, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-def test_exhaustive_bf16_value_and_tile_amax_pairs(gs, fmt):
-    """Every pair (x, amax) of bf16 patterns with |x| <= amax: one tile per
-    127 x-values holding amax itself, so each tile's scale comes from that
-    amax.  Covers the fast exact-quotient path for every finite amax and the
-    IEEE path for Inf/NaN amax; compared with the library composition of the
-    same formula on the device (itself pinned to the oracle on the CPU)."""
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_exhaustive_16bit_value_and_tile_amax_pairs(gs, fmt, dt):
+    """Every pair (x, amax) of 16-bit patterns (bf16 or f16) with |x| <= amax:
+    one tile per 127 x-values holding amax itself, so each tile's scale comes
+    from that amax.  Covers the fast exact-quotient path for every finite amax
+    and the IEEE path for Inf/NaN amax; compared with the library composition
+    of the same formula on the device (itself pinned to the oracle on the
+    CPU)."""
     chunk = 512
     for a0 in range(0, 0x8000, chunk):
         a = torch.arange(a0, min(a0 + chunk, 0x8000), device=DEV, dtype=torch.int64)
@@ -204,7 +206,7 @@ def test_exhaustive_bf16_value_and_tile_amax_pairs(gs, fmt):
         mag = torch.where(valid, pos % (am + 1), torch.zeros_like(pos))
         body = torch.where(valid, sign | mag, torch.zeros_like(pos))
         tiles = torch.cat([tile_a[:, None], body], dim=1).to(torch.int32).to(torch.int16)
-        xd = tiles.view(torch.bfloat16).contiguous()
+        xd = tiles.view(TDT[dt]).contiguous()
         n_t = xd.shape[0]
         q = torch.empty(n_t, 128, dtype=torch.uint8, device=DEV)
         s = torch.empty(n_t, 1, dtype=torch.float32, device=DEV)

@@ -1,0 +1,85 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C sources (on the
+CPU), builds it, and runs the CPU pin suite against that build: at least one
+pin must fail.  The unmodified sources must pass the same suite."""
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+from conftest import ROOT
+
+ORACLE = os.path.join(ROOT, "oracle")
+PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_scaler.py", "tests/test_oracle_quant.py"]
+
+MUTANTS = {
+    "ties round up instead of to even": (
+        "fp_formats.c", "(frac == 0.5 && fmod(lo, 2.0) != 0.0)", "(frac == 0.5)"),
+    "subnormal quantum dropped": (
+        "fp_formats.c", "if (e < emin) e = emin;", ""),
+    "E4M3 treated as IEEE-style (Inf, 7 NaNs)": (
+        "fp_formats.c", "FMT_E4M3 = {4, 3, 7, 0}", "FMT_E4M3 = {4, 3, 7, 1}"),
+    "E5M2 bias off by one": (
+        "fp_formats.c", "FMT_E5M2 = {5, 2, 15, 1}", "FMT_E5M2 = {5, 2, 16, 1}"),
+    "saturation code is the NaN pattern": (
+        "fp_formats.c", "return (emask << f->mbits) | (mmask - 1);", "return (emask << f->mbits) | mmask;"),
+    "growth test strict": (
+        "gradscaler.c", "if (*growth_tracker >= growth_interval)", "if (*growth_tracker > growth_interval)"),
+    "tracker not reset on overflow": (
+        "gradscaler.c", "*scale = *scale * backoff_factor;\n    *growth_tracker = 0;",
+        "*scale = *scale * backoff_factor;"),
+    "inf check misses NaN": (
+        "gradscaler.c", "if (isinf(v) || isnan(v)) found = 1;", "if (isinf(v)) found = 1;"),
+    "amax floor dropped": (
+        "fp8_quant.c", "if (!isnan(a) && a < floor_amax) a = floor_amax;", ""),
+    "quotient by reciprocal": (
+        "fp8_quant.c", "float v = x / s;", "float v = x * (1.0f / s);"),
+    "block scales transposed": (
+        "fp8_quant.c", "scales[bi * nbc + bj] = s;", "scales[bj * (R / br) + bi] = s;"),
+    "amax skips NaN": (
+        "fp8_quant.c", "if (isnan(v)) return NAN;", "if (isnan(v)) continue;"),
+    "dequant scale index transposed": (
+        "fp8_quant.c", "float s = scales[(r / br) * nbc + c / bc];", "float s = scales[(c / bc) * (R / br) + r / br];"),
+}
+
+
+def _build_variant(tmp, name, patch):
+    d = os.path.join(tmp, name.replace(" ", "_").replace("(", "").replace(")", "").replace(",", ""))
+    os.makedirs(d)
+    for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c"]:
+        shutil.copy(os.path.join(ORACLE, f), d)
+    if patch is not None:
+        fname, old, new = patch
+        path = os.path.join(d, fname)
+        src = open(path).read()
+        assert src.count(old) == 1, f"mutation anchor not unique/found: {old!r}"
+        open(path, "w").write(src.replace(old, new))
+    lib = os.path.join(d, "liboracle.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                    "-shared", "-o", lib, *[os.path.join(d, f) for f in
+                                            ["fp_formats.c", "gradscaler.c", "fp8_quant.c"]], "-lm"],
+                   check=True)
+    return lib
+
+
+def _run_pins(lib):
+    env = dict(os.environ, GS_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "-m", "not gpu", *PINS], cwd=ROOT, env=env, capture_output=True, text=True)
+    return r.returncode
+
+
+def test_pins_catch_every_planted_mistake():
+    with tempfile.TemporaryDirectory() as tmp:
+        cases = {"unmodified": None, **MUTANTS}
+        libs = {name: _build_variant(tmp, name, patch) for name, patch in cases.items()}
+        with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
+            rc = dict(zip(libs, ex.map(_run_pins, libs.values())))
+    assert rc.pop("unmodified") == 0, "the pins must pass on the unmodified oracle"
+    survived = [name for name, code in rc.items() if code == 0]
+    assert not survived, f"mistakes no pin caught: {survived}"

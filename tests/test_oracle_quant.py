@@ -178,3 +178,34 @@ def test_dequant_bf16_output_rounds_fp32_product(orc):
     y16 = orc.dequant(q, s, 1, 128, E4M3, out_dtype=BF16)
     lib = torch.from_numpy(y32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert (y16 == lib).all()
+
+
+@pytest.mark.parametrize("fmt,tdt", [(E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)])
+def test_quotient_is_the_ieee_division(orc, fmt, tdt):
+    """The pages quantise x / s.  Where the IEEE fp32 quotient and the product
+    x * fp32(1/s) straddle an FP8 rounding boundary they give different
+    codes; collect such (x, s) pairs from the bf16 domain (numpy's IEEE
+    division, torch's FP8 cast) and check the oracle follows the division."""
+    mx = np.float32(orc.fp8_max(fmt))
+    rng = np.random.default_rng(21 + fmt)
+    # random finite bf16 magnitudes as block amax values
+    amax_bits = rng.integers(0x0080, 0x7F7F, size=400).astype(np.uint32)
+    all_bits = np.arange(0x7F80, dtype=np.uint32)            # finite non-negative bf16
+    xs, ss = [], []
+    for ab in amax_bits:
+        amax = (ab << 16).view(np.float32)
+        s = np.maximum(amax, np.float32(1e-12)) / mx           # IEEE fp32 division
+        mags = all_bits[all_bits <= ab]
+        x = np.concatenate([(mags << 16).view(np.float32), -(mags << 16).view(np.float32)])
+        with np.errstate(over="ignore", under="ignore"):
+            qd = torch.from_numpy(np.clip(x / s, -mx, mx)).to(tdt).view(torch.uint8).numpy()
+            qm = torch.from_numpy(np.clip(x * (np.float32(1) / s), -mx, mx)).to(tdt).view(torch.uint8).numpy()
+        diff = np.flatnonzero(qd != qm)
+        xs.append(x[diff])
+        ss.append(np.full(diff.size, s, np.float32))
+    xs, ss = np.concatenate(xs), np.concatenate(ss)
+    assert xs.size >= 20, "the search must find boundary cases"
+    with np.errstate(over="ignore", under="ignore"):
+        want = torch.from_numpy(np.clip(xs / ss, -mx, mx)).to(tdt).view(torch.uint8).numpy()
+    got = np.array([orc.quant_one(float(x), float(s), fmt) for x, s in zip(xs, ss)], np.uint8)
+    assert (got == want).all()
