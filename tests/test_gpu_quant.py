@@ -83,6 +83,8 @@ def test_quant_128x128_shapes(gs, orc, fmt, dt, R, C):
     rng = np.random.default_rng(R * 3 + C)
     xh, xd = _host_input(rng, R, C, dt, special=True)
     _check_block(gs, orc, xh, xd, dt, 128, 128, fmt)
+    if dt != "f32":   # the same block with 8-byte-aligned codes (the TMA path)
+        _check_block(gs, orc, xh, xd, dt, 128, 128, fmt, q_off=8)
 
 
 @pytest.mark.parametrize("br", [1, 128])
