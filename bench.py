@@ -60,7 +60,7 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--only", choices=["unscale", "quant_1x128", "dequant", "quant_128x128",
-                                      "quant_tensor"],
+                                      "quant_tensor", "quant_mx", "dequant_mx"],
                    help="time one kernel alone on a small case (for ncu captures)")
     return p.parse_args(argv)
 
@@ -567,6 +567,19 @@ def run_only(args):
         else:
             fn = lambda: gs.fp8_dequant(q, s, 1, 128, "e4m3", y)
         nbytes = 3 * a.numel + 4 * (a.numel // 128)
+    elif args.only in ("quant_mx", "dequant_mx"):
+        a = wl.cfg3_act()
+        x = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
+        dg.fill_device(a.spec, 0, a.numel, x.data_ptr(), st)
+        q = torch.empty(a.rows, a.cols, dtype=torch.uint8, device=dev)
+        s = torch.empty(a.rows, a.cols // 32, dtype=torch.uint8, device=dev)
+        y = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
+        gs.fp8_quant_mx(x, "e4m3", q, s)
+        if args.only == "quant_mx":
+            fn = lambda: gs.fp8_quant_mx(x, "e4m3", q, s)
+        else:
+            fn = lambda: gs.fp8_dequant_mx(q, s, "e4m3", y)
+        nbytes = 3 * a.numel + a.numel // 32
     elif args.only == "quant_128x128":
         w = wl.cfg4_weight()
         x = torch.empty(w.rows, w.cols, dtype=torch.bfloat16, device=dev)

@@ -208,6 +208,29 @@ int fp8_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C, int
                 int32_t block_c, int fmt, int out_dtype, void* y, void* stream);
 
 /* ------------------------------------------------------------------------
+ * MXFP8: one power-of-two scale per 32 consecutive elements ([P5] "FP8
+ * training": Blackwell's MX formats keep one scaling factor per 32 elements
+ * in hardware).  The pages give only the block size; the scale rule is the
+ * OCP Microscaling convention: an E8M0 byte c means 2^(c - 127) (255 is
+ * NaN); for each 1x32 block, e = floor(log2(amax)) - emax_elem (8 for E4M3,
+ * 15 for E5M2), clamped to [-127, 127], e = -127 for an all-zero block;
+ * q = fp8(x * 2^-e), round to nearest even, saturating at +-MAX; a block
+ * holding Inf or NaN gets scale 255 and codes 0x7F.
+ * --------------------------------------------------------------------- */
+
+/* x: row-major [R, C] of in_dtype (GS_BF16 / GS_F16 / GS_F32), C % 32 == 0
+ * (else GS_ERR_SHAPE); q: R*C FP8 codes; scales: R*C/32 E8M0 bytes,
+ * row-major [R, C/32].  Buffers 32-byte aligned with 16-bit input take the
+ * vectorised path; any element-aligned buffers are accepted. */
+int fp8_quant_mx(const void* x, int in_dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
+                 uint8_t* scales, void* stream);
+
+/* y = decode(q) * 2^(scale - 127) in fp32, stored as fp32 or rounded to
+ * nearest-even bfloat16 (out_dtype GS_F32 / GS_BF16). */
+int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C, int fmt,
+                   int out_dtype, void* y, void* stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  * --------------------------------------------------------------------- */
 

@@ -20,7 +20,7 @@ __all__ = [
     "gs_status_str", "gs_version", "gs_tensor_list_create", "gs_unscale_check_update",
     "gs_scaler_state_get", "gs_scaler_state_set", "fp8_quant_block", "fp8_quant_tensor",
     "fp8_dequant", "gs_ws_bytes", "gs_device_status", "lib_path",
-    "gs_unscale_check_update_noalloc", "gs_noalloc_limits",
+    "gs_unscale_check_update_noalloc", "gs_noalloc_limits", "fp8_quant_mx", "fp8_dequant_mx",
 ]
 
 GS_OK, GS_ERR_NULL, GS_ERR_SHAPE, GS_ERR_DTYPE, GS_ERR_ARG, GS_ERR_CUDA, GS_ERR_TIMEOUT = range(7)
@@ -59,6 +59,8 @@ def _load_lib() -> ctypes.CDLL:
         "fp8_quant_tensor": (ci, [vp, ci, i64, ci, vp, vp, vp, vp]),
         "fp8_dequant": (ci, [vp, vp, i64, i64, i32, i32, ci, ci, vp, vp]),
         "gs_device_status": (ci, [ctypes.POINTER(i32), vp]),
+        "fp8_quant_mx": (ci, [vp, ci, i64, i64, ci, vp, vp, vp]),
+        "fp8_dequant_mx": (ci, [vp, vp, i64, i64, ci, ci, vp, vp]),
         "gs_unscale_check_update_noalloc": (ci, [vp, vp, vp, i32, vp, vp, vp, vp, f32, f32, i32, vp]),
         "gs_noalloc_limits": (ci, [ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64)]),
     }
@@ -238,6 +240,21 @@ def fp8_dequant(q: torch.Tensor, scales: torch.Tensor, block_r: int, block_c: in
     R, C = q.shape
     _check(_lib.fp8_dequant(_ptr(q), _ptr(scales), R, C, block_r, block_c, _FMTS[fmt],
                             _DTYPES[y.dtype], _ptr(y), _stream(stream)), "fp8_dequant")
+
+
+def fp8_quant_mx(x: torch.Tensor, fmt, q: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """x: [R, C] (C % 32 == 0) bf16 / f16 / f32; q: uint8 [R, C]; scales: uint8 [R, C/32]."""
+    _contig(x, "x")
+    R, C = x.shape
+    _check(_lib.fp8_quant_mx(_ptr(x), _DTYPES[x.dtype], R, C, _FMTS[fmt], _ptr(q), _ptr(scales),
+                             _stream(stream)), "fp8_quant_mx")
+
+
+def fp8_dequant_mx(q: torch.Tensor, scales: torch.Tensor, fmt, y: torch.Tensor, stream=None) -> None:
+    _contig(q, "q")
+    R, C = q.shape
+    _check(_lib.fp8_dequant_mx(_ptr(q), _ptr(scales), R, C, _FMTS[fmt], _DTYPES[y.dtype], _ptr(y),
+                               _stream(stream)), "fp8_dequant_mx")
 
 
 def gs_device_status(stream=None) -> int:

@@ -294,6 +294,38 @@ int fp8_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C, int
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
 
+int fp8_quant_mx(const void* x, int in_dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
+                 uint8_t* scales, void* stream) {
+  if (!valid_dtype(in_dtype) || !valid_fmt(fmt)) return GS_ERR_DTYPE;
+  if (R < 0 || C < 0 || !mul_ok(R, C) || !mul_ok(R * C, 4)) return GS_ERR_SHAPE;
+  if (C % 32 != 0) return GS_ERR_SHAPE;
+  if (R == 0 || C == 0) return GS_OK;
+  if (!x || !q || !scales) return GS_ERR_NULL;
+  const size_t n = (size_t)(R * C), esz = dtype_size(in_dtype), ns = n / 32;
+  if (!aligned(x, esz)) return GS_ERR_ARG;
+  if (!device_reachable(x) || !device_reachable(q) || !device_reachable(scales)) return GS_ERR_ARG;
+  if (overlaps(x, n * esz, q, n) || overlaps(x, n * esz, scales, ns) || overlaps(q, n, scales, ns))
+    return GS_ERR_ARG;
+  cudaError_t e = launch_quant_mx(x, in_dtype, R, C, fmt, q, scales, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C, int fmt,
+                   int out_dtype, void* y, void* stream) {
+  if (!valid_fmt(fmt) || !(out_dtype == GS_F32 || out_dtype == GS_BF16)) return GS_ERR_DTYPE;
+  if (R < 0 || C < 0 || !mul_ok(R, C) || !mul_ok(R * C, 4)) return GS_ERR_SHAPE;
+  if (C % 32 != 0) return GS_ERR_SHAPE;
+  if (R == 0 || C == 0) return GS_OK;
+  if (!q || !scales || !y) return GS_ERR_NULL;
+  const size_t n = (size_t)(R * C), ysz = out_dtype == GS_F32 ? 4 : 2;
+  if (!aligned(y, ysz)) return GS_ERR_ARG;
+  if (!device_reachable(q) || !device_reachable(scales) || !device_reachable(y)) return GS_ERR_ARG;
+  if (overlaps(y, n * ysz, q, n) || overlaps(y, n * ysz, scales, n / 32)) return GS_ERR_ARG;
+  cudaError_t e = launch_dequant_mx(q, scales, R, C, fmt, out_dtype, y,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
 int gs_device_status(int32_t* h_status, void* stream) {
   if (!h_status) return GS_ERR_NULL;
   int32_t* p = device_status_ptr();

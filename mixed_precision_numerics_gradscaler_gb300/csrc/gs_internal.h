@@ -50,6 +50,10 @@ cudaError_t launch_quant_tensor(const void* x, int dtype, int64_t n, int fmt, ui
 cudaError_t launch_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C,
                            int block_r, int block_c, int fmt, int out_dtype, void* y,
                            cudaStream_t stream);
+cudaError_t launch_quant_mx(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
+                            uint8_t* scales, cudaStream_t stream);
+cudaError_t launch_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C,
+                              int fmt, int out_dtype, void* y, cudaStream_t stream);
 cudaError_t launch_set_state(float* scale, int32_t* tracker, float h_scale, int32_t h_tracker,
                              cudaStream_t stream);
 

@@ -18,7 +18,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SOURCES = ["fp_formats.c", "gradscaler.c", "fp8_quant.c"]
+_SOURCES = ["fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c"]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,10 @@ def _load():
             "orc_amax": (ctypes.c_float, [vp, ctypes.c_int, i64]),
             "orc_scale_from_amax": (ctypes.c_float, [ctypes.c_float, ctypes.c_int]),
             "orc_quant_one": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_float, ctypes.c_int]),
+            "orc_e8m0_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "orc_mx_scale_code": (i32, [ctypes.c_double, ctypes.c_int]),
+            "orc_quant_mx": (None, [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp]),
+            "orc_dequant_mx": (None, [vp, vp, i64, i64, ctypes.c_int, ctypes.c_int, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -244,3 +248,34 @@ def scale_from_amax(a: float, fmt: int) -> float:
 
 def quant_one(x: float, s: float, fmt: int) -> int:
     return _load().orc_quant_one(x, s, fmt)
+
+
+# ---- MXFP8 -----------------------------------------------------------------
+
+def e8m0_decode(c: int) -> float:
+    return _load().orc_e8m0_decode(c)
+
+
+def mx_scale_code(amax: float, fmt: int) -> int:
+    return _load().orc_mx_scale_code(amax, fmt)
+
+
+def quant_mx(x: np.ndarray, fmt: int, dtype: int | None = None):
+    """Row-major [R, C] (C % 32 == 0) -> (uint8 codes [R, C], E8M0 scales [R, C/32])."""
+    x = np.ascontiguousarray(x)
+    code = _dtype_code(x, dtype)
+    R, C = x.shape
+    assert C % 32 == 0
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R, C // 32), np.uint8)
+    _load().orc_quant_mx(_ptr(x), code, R, C, fmt, _ptr(q), _ptr(s))
+    return q, s
+
+
+def dequant_mx(q: np.ndarray, scales: np.ndarray, fmt: int, out_dtype: int = F32) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    R, C = q.shape
+    y = np.empty((R, C), np.float32 if out_dtype == F32 else np.uint16)
+    _load().orc_dequant_mx(_ptr(q), _ptr(scales), R, C, fmt, out_dtype, _ptr(y))
+    return y

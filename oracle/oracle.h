@@ -85,6 +85,15 @@ void orc_quant_tensor(const void* x, int dtype, int64_t n, int fmt,
 void orc_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C,
                  int64_t br, int64_t bc, int fmt, int out_dtype, void* y);
 
+/* ---- MXFP8: one power-of-two (E8M0) scale per 32 consecutive elements
+ *      ([P5] "FP8 training", the MX formats sentence; see mx_quant.c) ---- */
+double  orc_e8m0_decode(uint8_t c);
+int32_t orc_mx_scale_code(double amax, int fmt);
+void orc_quant_mx(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
+                  uint8_t* scales);
+void orc_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C, int fmt,
+                    int out_dtype, void* y);
+
 /* Pieces of the block path, exposed so tests can pin each step. */
 float orc_amax(const void* x, int dtype, int64_t n);          /* NaN-propagating */
 float orc_scale_from_amax(float amax, int fmt);               /* max(a,1e-12)/MAX */

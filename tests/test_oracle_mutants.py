@@ -15,7 +15,8 @@ import pytest
 from conftest import ROOT
 
 ORACLE = os.path.join(ROOT, "oracle")
-PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_scaler.py", "tests/test_oracle_quant.py"]
+PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_scaler.py", "tests/test_oracle_quant.py",
+        "tests/test_oracle_mx.py"]
 
 MUTANTS = {
     "ties round up instead of to even": (
@@ -43,6 +44,11 @@ MUTANTS = {
         "fp8_quant.c", "scales[bi * nbc + bj] = s;", "scales[bj * (R / br) + bi] = s;"),
     "amax skips NaN": (
         "fp8_quant.c", "if (isnan(v)) return NAN;", "if (isnan(v)) continue;"),
+    "MX emax of E4M3 off by one": (
+        "mx_quant.c", "return fmt == ORC_E5M2 ? 15 : 8;", "return fmt == ORC_E5M2 ? 15 : 7;"),
+    "MX scale applied the wrong way": (
+        "mx_quant.c", "ldexp(orc__load_elem(x, dtype, base + i), 127 - code)",
+        "ldexp(orc__load_elem(x, dtype, base + i), code - 127)"),
     "dequant scale index transposed": (
         "fp8_quant.c", "float s = scales[(r / br) * nbc + c / bc];", "float s = scales[(c / bc) * (R / br) + r / br];"),
 }
@@ -51,7 +57,7 @@ MUTANTS = {
 def _build_variant(tmp, name, patch):
     d = os.path.join(tmp, name.replace(" ", "_").replace("(", "").replace(")", "").replace(",", ""))
     os.makedirs(d)
-    for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c"]:
+    for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c"]:
         shutil.copy(os.path.join(ORACLE, f), d)
     if patch is not None:
         fname, old, new = patch
@@ -62,7 +68,8 @@ def _build_variant(tmp, name, patch):
     lib = os.path.join(d, "liboracle.so")
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
                     "-shared", "-o", lib, *[os.path.join(d, f) for f in
-                                            ["fp_formats.c", "gradscaler.c", "fp8_quant.c"]], "-lm"],
+                                            ["fp_formats.c", "gradscaler.c", "fp8_quant.c",
+                                             "mx_quant.c"]], "-lm"],
                    check=True)
     return lib
 
