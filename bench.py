@@ -60,7 +60,7 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--only", choices=["unscale", "quant_1x128", "dequant", "quant_128x128",
-                                      "quant_tensor", "quant_mx", "dequant_mx"],
+                                      "quant_tensor", "quant_mx", "dequant_mx", "quant_delayed"],
                    help="time one kernel alone on a small case (for ncu captures)")
     return p.parse_args(argv)
 
@@ -588,6 +588,17 @@ def run_only(args):
         s = torch.empty(w.rows // 128, w.cols // 128, dtype=torch.float32, device=dev)
         fn = lambda: gs.fp8_quant_block(x, 128, 128, "e4m3", q, s)
         nbytes = 3 * w.numel + 4 * (w.numel // 16384)
+    elif args.only == "quant_delayed":
+        g = wl.cfg4_grad()
+        x = torch.empty(g.numel, dtype=torch.bfloat16, device=dev)
+        dg.fill_device(g.spec, 0, g.numel, x.data_ptr(), st)
+        q = torch.empty(g.numel, dtype=torch.uint8, device=dev)
+        hist = torch.full((16,), 1e-2, dtype=torch.float32, device=dev)
+        pos = torch.zeros(1, dtype=torch.int32, device=dev)
+        used = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=dev)
+        fn = lambda: gs.fp8_quant_tensor_delayed(x, "e5m2", q, hist, pos, used, ws)
+        nbytes = 3 * g.numel + 4
     else:
         g = wl.cfg4_grad()
         x = torch.empty(g.numel, dtype=torch.bfloat16, device=dev)

@@ -120,6 +120,25 @@ int gs_unscale_check_update(const gs_tensor_list* list, float* scale, int32_t* g
                             int32_t* found_inf, int64_t* skipped, float growth_factor,
                             float backoff_factor, int32_t growth_interval, void* stream);
 
+/* The same step under a loss-scale policy with hysteresis ([P3] DeepSpeed
+ * paragraph: loss_scale_window 1000, hysteresis 2, consecutive_hysteresis
+ * false, min_loss_scale 1 -- the pages name the settings; this reading is
+ * the library's): on an overflow the step is skipped, the window restarts
+ * (growth_tracker = 0) and, while *hysteresis_state > 1, one unit of it is
+ * spent and S kept; with one unit left, S = max(S * backoff_factor,
+ * min_scale).  A clean step advances the window; a full window
+ * (growth_tracker reaching `window`) multiplies S by growth_factor and
+ * restores *hysteresis_state to `hysteresis`; with consecutive_hysteresis
+ * != 0 it is restored after every clean step instead.  hysteresis_state is
+ * a device int32 the caller initialises to `hysteresis`.  hysteresis = 1
+ * and min_scale = 0 give exactly gs_unscale_check_update. */
+int gs_unscale_check_update_hysteresis(const gs_tensor_list* list, float* scale,
+                                       int32_t* growth_tracker, int32_t* hysteresis_state,
+                                       int32_t* found_inf, int64_t* skipped, float growth_factor,
+                                       float backoff_factor, int32_t window, int32_t hysteresis,
+                                       int32_t consecutive_hysteresis, float min_scale,
+                                       void* stream);
+
 /* Checkpoint support: the scaler's whole state is {S, growth_tracker}.
  * get: copies the two device scalars to host variables and waits for the
  *      copy on `stream` (this call synchronises that stream).
@@ -198,6 +217,22 @@ size_t gs_ws_bytes(void);
  * Calls sharing one ws must be ordered on one stream. */
 int fp8_quant_tensor(const void* x, int in_dtype, int64_t n, int fmt, uint8_t* q, float* scale,
                      void* ws, void* stream);
+
+/* Per-tensor quantisation with delayed scaling ([P4] "Failure 1": keep a
+ * short history of recent max-abs values and derive s from it; [P5] "FP8
+ * training" figure: per tensor, delayed, from recent amax).  One pass over
+ * x: the scale applied is s = max(max|amax_history|, 1e-12) / MAX (written
+ * to *scale_used); q = fp8(clamp(x / s)); then amax(x) is written at
+ * amax_history[*history_pos] and *history_pos advances modulo
+ * history_len (1..65536).  amax_history (fp32), history_pos (int32) and
+ * scale_used are device memory the caller owns and initialises (a zero
+ * history gives the floor scale: everything non-tiny saturates on the
+ * first step).  ws: >= gs_ws_bytes() bytes of device scratch.  A NaN in the
+ * history makes the scale NaN (every code 0x7F) until it leaves the
+ * window.  Calls sharing a history or ws must be ordered on one stream. */
+int fp8_quant_tensor_delayed(const void* x, int in_dtype, int64_t n, int fmt, uint8_t* q,
+                             float* amax_history, int32_t history_len, int32_t* history_pos,
+                             float* scale_used, void* ws, void* stream);
 
 /* Dequantise: y = decode(q) * s (fp32 product), stored as fp32 or rounded
  * to nearest-even bfloat16 (out_dtype GS_F32 or GS_BF16).

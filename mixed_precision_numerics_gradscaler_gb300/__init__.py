@@ -21,6 +21,7 @@ __all__ = [
     "gs_scaler_state_get", "gs_scaler_state_set", "fp8_quant_block", "fp8_quant_tensor",
     "fp8_dequant", "gs_ws_bytes", "gs_device_status", "lib_path",
     "gs_unscale_check_update_noalloc", "gs_noalloc_limits", "fp8_quant_mx", "fp8_dequant_mx",
+    "gs_unscale_check_update_hysteresis", "fp8_quant_tensor_delayed",
 ]
 
 GS_OK, GS_ERR_NULL, GS_ERR_SHAPE, GS_ERR_DTYPE, GS_ERR_ARG, GS_ERR_CUDA, GS_ERR_TIMEOUT = range(7)
@@ -59,6 +60,9 @@ def _load_lib() -> ctypes.CDLL:
         "fp8_quant_tensor": (ci, [vp, ci, i64, ci, vp, vp, vp, vp]),
         "fp8_dequant": (ci, [vp, vp, i64, i64, i32, i32, ci, ci, vp, vp]),
         "gs_device_status": (ci, [ctypes.POINTER(i32), vp]),
+        "gs_unscale_check_update_hysteresis": (ci, [vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32,
+                                                    f32, vp]),
+        "fp8_quant_tensor_delayed": (ci, [vp, ci, i64, ci, vp, vp, i32, vp, vp, vp, vp]),
         "fp8_quant_mx": (ci, [vp, ci, i64, i64, ci, vp, vp, vp]),
         "fp8_dequant_mx": (ci, [vp, vp, i64, i64, ci, ci, vp, vp]),
         "gs_unscale_check_update_noalloc": (ci, [vp, vp, vp, i32, vp, vp, vp, vp, f32, f32, i32, vp]),
@@ -200,6 +204,29 @@ def gs_noalloc_limits() -> tuple[int, int, int]:
     _check(_lib.gs_noalloc_limits(ctypes.byref(t), ctypes.byref(c), ctypes.byref(e)),
            "gs_noalloc_limits")
     return t.value, c.value, e.value
+
+
+def gs_unscale_check_update_hysteresis(tlist: TensorList, scale: torch.Tensor,
+                                       growth_tracker: torch.Tensor, hysteresis_state: torch.Tensor,
+                                       found_inf: torch.Tensor, skipped: torch.Tensor | None = None,
+                                       growth_factor: float = 2.0, backoff_factor: float = 0.5,
+                                       window: int = 1000, hysteresis: int = 2,
+                                       consecutive_hysteresis: bool = False, min_scale: float = 1.0,
+                                       stream=None) -> None:
+    _check(_lib.gs_unscale_check_update_hysteresis(
+        tlist.handle, _ptr(scale), _ptr(growth_tracker), _ptr(hysteresis_state), _ptr(found_inf),
+        _ptr(skipped), growth_factor, backoff_factor, window, hysteresis,
+        int(consecutive_hysteresis), min_scale, _stream(stream)), "gs_unscale_check_update_hysteresis")
+
+
+def fp8_quant_tensor_delayed(x: torch.Tensor, fmt, q: torch.Tensor, amax_history: torch.Tensor,
+                             history_pos: torch.Tensor, scale_used: torch.Tensor, ws: torch.Tensor,
+                             stream=None) -> None:
+    _contig(x, "x")
+    _check(_lib.fp8_quant_tensor_delayed(_ptr(x), _DTYPES[x.dtype], x.numel(), _FMTS[fmt], _ptr(q),
+                                         _ptr(amax_history), amax_history.numel(), _ptr(history_pos),
+                                         _ptr(scale_used), _ptr(ws), _stream(stream)),
+           "fp8_quant_tensor_delayed")
 
 
 def gs_scaler_state_get(scale: torch.Tensor, growth_tracker: torch.Tensor,

@@ -1,0 +1,199 @@
+// fp8_delayed.cu -- per-tensor FP8 quantisation with delayed scaling ("Why
+// FP8 training is stable", "Failure 1": keep a short history of recent
+// max-abs values and derive s from it; "Mixed precision and FP8 training",
+// "FP8 training" figure: per tensor, delayed, from recent amax).
+//
+// The scale of this step comes from the history, so one pass reads x once:
+//   s = max(max|history|, 1e-12) / MAX        (every CTA, from device memory)
+//   q = fp8(clamp(x / s))                      (exact quotient, RNE, saturating)
+//   partial amax of x per CTA                  (integer max of magnitude bits)
+// and a one-CTA kernel then writes amax(x) at history[pos] and advances
+// pos.  3 bytes per 16-bit element instead of current scaling's 5.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+constexpr int kDelThreads = 256;
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0;
+#pragma unroll
+  for (int w = 0; w < kDelThreads / 32; ++w) m = max(m, red[w]);
+  __syncthreads();
+  return m;
+}
+
+// Max |h| over the history as an fp32 bit pattern; NaN entries win (their
+// magnitude patterns order above every number).
+__device__ __forceinline__ uint32_t history_max_bits(const float* history, int hist_len,
+                                                     uint32_t* red) {
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < hist_len; i += blockDim.x)
+    m = max(m, __float_as_uint(history[i]) & 0x7FFFFFFFu);
+  return block_max_u32(m, red);
+}
+
+template <typename Tag, int FMT>
+__global__ void __launch_bounds__(kDelThreads)
+    quant_delayed_v8(const uint8_t* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
+                     const float* __restrict__ history, int hist_len, float* scale_used,
+                     uint32_t* __restrict__ partials) {
+  __shared__ uint32_t red[kDelThreads / 32];
+  constexpr int kSteps = QuotSteps<Tag>::value;
+  const float s = block_scale<FMT>(__uint_as_float(history_max_bits(history, hist_len, red)));
+  const bool fin = isfinite(s);
+  const float r = __frcp_rn(s);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_used = s;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t nv = n >> 4;  // 16 elements (32 bytes) per vector
+  const uint32_t mm = 0x7FFF7FFFu;
+  uint32_t m2 = 0;
+  int64_t v = tid;
+  for (; v + nthreads < nv; v += 2 * nthreads) {
+    const V8 a = ld_stream8(x + 32 * v), b = ld_stream8(x + 32 * (v + nthreads));
+    uint32_t pa[4], pb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.w[2 * j] & mm, a.w[2 * j + 1] & mm),
+                                 __vmaxu2(b.w[2 * j] & mm, b.w[2 * j + 1] & mm)));
+      pa[j] = quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j]), lo16<Tag>(a.w[2 * j]), s, r, fin) |
+              (quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j + 1]), lo16<Tag>(a.w[2 * j + 1]), s, r,
+                                       fin)
+               << 16);
+      pb[j] = quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j]), lo16<Tag>(b.w[2 * j]), s, r, fin) |
+              (quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j + 1]), lo16<Tag>(b.w[2 * j + 1]), s, r,
+                                       fin)
+               << 16);
+    }
+    st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(pa[0], pa[1], pa[2], pa[3]));
+    st_stream(reinterpret_cast<uint4*>(q + 16 * (v + nthreads)), make_uint4(pb[0], pb[1], pb[2], pb[3]));
+  }
+  for (; v < nv; v += nthreads) {
+    const V8 a = ld_stream8(x + 32 * v);
+    uint32_t pa[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m2 = __vmaxu2(m2, __vmaxu2(a.w[2 * j] & mm, a.w[2 * j + 1] & mm));
+      pa[j] = quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j]), lo16<Tag>(a.w[2 * j]), s, r, fin) |
+              (quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j + 1]), lo16<Tag>(a.w[2 * j + 1]), s, r,
+                                       fin)
+               << 16);
+    }
+    st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(pa[0], pa[1], pa[2], pa[3]));
+  }
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  // ragged tail (n not a multiple of 16)
+  const uint16_t* xs = reinterpret_cast<const uint16_t*>(x);
+  for (int64_t i = nv * 16 + tid; i < n; i += nthreads) {
+    const uint32_t h = xs[i];
+    m = max(m, h & 0x7FFFu);
+    const float f = std::is_same<Tag, BF16Tag>::value ? __uint_as_float(h << 16)
+                                                       : __half2float(__ushort_as_half((unsigned short)h));
+    q[i] = (uint8_t)(quant_pair<FMT, kSteps>(0.0f, f, s, r, fin) & 0xFFu);
+  }
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+// Any dtype and alignment, element by element.
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kDelThreads)
+    quant_delayed_any(const void* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
+                      const float* __restrict__ history, int hist_len, float* scale_used,
+                      uint32_t* __restrict__ partials) {
+  __shared__ uint32_t red[kDelThreads / 32];
+  const float s = block_scale<FMT>(__uint_as_float(history_max_bits(history, hist_len, red)));
+  const bool fin = isfinite(s);
+  const float r = __frcp_rn(s);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_used = s;
+  uint32_t m = 0;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += nthreads) {
+    float f;
+    uint32_t mag;
+    if constexpr (DT == GS_F32) {
+      f = reinterpret_cast<const float*>(x)[i];
+      mag = __float_as_uint(f) & 0x7FFFFFFFu;
+    } else {
+      const uint32_t h = reinterpret_cast<const uint16_t*>(x)[i];
+      f = DT == GS_BF16 ? __uint_as_float(h << 16) : __half2float(__ushort_as_half((unsigned short)h));
+      mag = h & 0x7FFFu;
+    }
+    m = max(m, mag);
+    q[i] = (uint8_t)(quant_pair<FMT, 2>(0.0f, f, s, r, fin) & 0xFFu);
+  }
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+// One CTA: amax of this step -> history[pos], pos = (pos + 1) % hist_len.
+template <int DT>
+__global__ void __launch_bounds__(kDelThreads)
+    delayed_record(const uint32_t* __restrict__ partials, int n_partials, float* history,
+                   int hist_len, int32_t* pos) {
+  __shared__ uint32_t red[kDelThreads / 32];
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < n_partials; i += blockDim.x) m = max(m, partials[i]);
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) {
+    float a;
+    if constexpr (DT == GS_F32) a = __uint_as_float(m);
+    else if constexpr (DT == GS_BF16) a = __uint_as_float(m << 16);
+    else a = __half2float(__ushort_as_half((unsigned short)m));
+    int p = *pos;
+    p = (p < 0 || p >= hist_len) ? 0 : p;
+    history[p] = a;
+    *pos = (p + 1) % hist_len;
+  }
+}
+
+template <int DT, int FMT>
+static cudaError_t delayed_t(const void* x, int64_t n, uint8_t* q, float* history, int hist_len,
+                             int32_t* pos, float* scale_used, uint32_t* partials, cudaStream_t st) {
+  int64_t grid = (n + kDelThreads * 32 - 1) / (kDelThreads * 32);
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (grid > cap) grid = cap;
+  if (grid > kMaxAmaxBlocks) grid = kMaxAmaxBlocks;
+  if (grid < 1) grid = 1;
+  if constexpr (DT != GS_F32) {
+    if (((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 15u) == 0) {
+      using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
+      quant_delayed_v8<Tag, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(
+          reinterpret_cast<const uint8_t*>(x), n, q, history, hist_len, scale_used, partials);
+    } else {
+      quant_delayed_any<DT, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(x, n, q, history, hist_len,
+                                                                         scale_used, partials);
+    }
+  } else {
+    quant_delayed_any<DT, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(x, n, q, history, hist_len,
+                                                                       scale_used, partials);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  delayed_record<DT><<<1, kDelThreads, 0, st>>>(partials, (int)grid, history, hist_len, pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tensor_delayed(const void* x, int dtype, int64_t n, int fmt, uint8_t* q,
+                                        float* history, int hist_len, int32_t* pos,
+                                        float* scale_used, uint32_t* partials, cudaStream_t st) {
+  if (fmt == GS_E4M3) {
+    if (dtype == GS_BF16) return delayed_t<GS_BF16, GS_E4M3>(x, n, q, history, hist_len, pos, scale_used, partials, st);
+    if (dtype == GS_F16) return delayed_t<GS_F16, GS_E4M3>(x, n, q, history, hist_len, pos, scale_used, partials, st);
+    return delayed_t<GS_F32, GS_E4M3>(x, n, q, history, hist_len, pos, scale_used, partials, st);
+  }
+  if (dtype == GS_BF16) return delayed_t<GS_BF16, GS_E5M2>(x, n, q, history, hist_len, pos, scale_used, partials, st);
+  if (dtype == GS_F16) return delayed_t<GS_F16, GS_E5M2>(x, n, q, history, hist_len, pos, scale_used, partials, st);
+  return delayed_t<GS_F32, GS_E5M2>(x, n, q, history, hist_len, pos, scale_used, partials, st);
+}
+
+}  // namespace gs

@@ -208,6 +208,32 @@ int gs_unscale_check_update(const gs_tensor_list* list, float* scale, int32_t* g
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
 
+int gs_unscale_check_update_hysteresis(const gs_tensor_list* list, float* scale,
+                                       int32_t* growth_tracker, int32_t* hysteresis_state,
+                                       int32_t* found_inf, int64_t* skipped, float growth_factor,
+                                       float backoff_factor, int32_t window, int32_t hysteresis,
+                                       int32_t consecutive_hysteresis, float min_scale,
+                                       void* stream) {
+  if (!list || !scale || !growth_tracker || !hysteresis_state || !found_inf) return GS_ERR_NULL;
+  if (window < 1 || hysteresis < 1) return GS_ERR_ARG;
+  if (!std::isfinite(growth_factor) || !(growth_factor > 0.0f) || !std::isfinite(backoff_factor) ||
+      !(backoff_factor > 0.0f) || !std::isfinite(min_scale) || min_scale < 0.0f)
+    return GS_ERR_ARG;
+  if (list->device != current_device()) return GS_ERR_ARG;
+  if (!aligned(scale, 4) || !aligned(growth_tracker, 4) || !aligned(hysteresis_state, 4) ||
+      !aligned(found_inf, 4) || (skipped && !aligned(skipped, 8)))
+    return GS_ERR_ARG;
+  if (!device_reachable(scale) || !device_reachable(growth_tracker) ||
+      !device_reachable(hysteresis_state) || !device_reachable(found_inf) ||
+      (skipped && !device_reachable(skipped)))
+    return GS_ERR_ARG;
+  cudaError_t e = launch_unscale_check_update(
+      list->d_chunks, list->n_chunks, list->d_ws, scale, growth_tracker, found_inf, skipped,
+      growth_factor, backoff_factor, window, static_cast<cudaStream_t>(stream),
+      ScalerPolicy{hysteresis_state, hysteresis, consecutive_hysteresis ? 1 : 0, min_scale});
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
 int gs_scaler_state_get(const float* scale, const int32_t* growth_tracker, float* h_scale,
                         int32_t* h_growth_tracker, void* stream) {
   if (!scale || !growth_tracker || !h_scale || !h_growth_tracker) return GS_ERR_NULL;
@@ -291,6 +317,34 @@ int fp8_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C, int
   if (overlaps(y, n * ysz, q, n) || overlaps(y, n * ysz, scales, nscales * 4)) return GS_ERR_ARG;
   cudaError_t e = launch_dequant(q, scales, R, C, block_r, block_c, fmt, out_dtype, y,
                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int fp8_quant_tensor_delayed(const void* x, int in_dtype, int64_t n, int fmt, uint8_t* q,
+                             float* amax_history, int32_t history_len, int32_t* history_pos,
+                             float* scale_used, void* ws, void* stream) {
+  if (!valid_dtype(in_dtype) || !valid_fmt(fmt)) return GS_ERR_DTYPE;
+  if (n < 0 || !mul_ok(n, 4)) return GS_ERR_SHAPE;
+  if (history_len < 1 || history_len > 65536) return GS_ERR_ARG;
+  if (!amax_history || !history_pos || !scale_used || !ws || (n > 0 && (!x || !q)))
+    return GS_ERR_NULL;
+  const size_t esz = dtype_size(in_dtype), hb = (size_t)history_len * 4;
+  if (!aligned(amax_history, 4) || !aligned(history_pos, 4) || !aligned(scale_used, 4) ||
+      !aligned(ws, 4) || (n > 0 && !aligned(x, esz)))
+    return GS_ERR_ARG;
+  if (!device_reachable(amax_history) || !device_reachable(history_pos) ||
+      !device_reachable(scale_used) || !device_reachable(ws) ||
+      (n > 0 && (!device_reachable(x) || !device_reachable(q))))
+    return GS_ERR_ARG;
+  const size_t xb = (size_t)n * esz, wb = gs_ws_bytes();
+  if (overlaps(x, xb, q, (size_t)n) || overlaps(amax_history, hb, q, (size_t)n) ||
+      overlaps(amax_history, hb, x, xb) || overlaps(ws, wb, x, xb) || overlaps(ws, wb, q, (size_t)n) ||
+      overlaps(ws, wb, amax_history, hb) || overlaps(scale_used, 4, q, (size_t)n) ||
+      overlaps(scale_used, 4, amax_history, hb) || overlaps(history_pos, 4, amax_history, hb))
+    return GS_ERR_ARG;
+  cudaError_t e = launch_quant_tensor_delayed(x, in_dtype, n, fmt, q, amax_history, history_len,
+                                              history_pos, scale_used, static_cast<uint32_t*>(ws),
+                                              static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
 

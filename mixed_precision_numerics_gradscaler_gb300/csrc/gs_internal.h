@@ -27,6 +27,18 @@ struct ListWs {
   int32_t pad[2];
 };
 
+// Loss-scale policy applied by the last CTA of the unscale kernel.  With
+// hyst == nullptr it is the GradScaler loop; otherwise the hysteresis
+// policy: an overflow spends one unit of *hyst (S kept) until one is left,
+// then S = max(S * backoff, min_scale); a full clean window grows S and
+// restores *hyst (after every clean step when consecutive != 0).
+struct ScalerPolicy {
+  int32_t* hyst;
+  int32_t hysteresis;
+  int32_t consecutive;
+  float min_scale;
+};
+
 // Cached device properties of the current device.
 int sm_count();
 int current_device();
@@ -38,7 +50,8 @@ void record_cuda_error(cudaError_t e);
 cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks, ListWs* ws,
                                         float* scale, int32_t* tracker, int32_t* found,
                                         int64_t* skipped, float growth, float backoff,
-                                        int32_t interval, cudaStream_t stream);
+                                        int32_t interval, cudaStream_t stream,
+                                        ScalerPolicy policy = ScalerPolicy{nullptr, 1, 0, 0.0f});
 
 cudaError_t launch_quant_1x128(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
                                float* scales, cudaStream_t stream);
@@ -54,6 +67,9 @@ cudaError_t launch_quant_mx(const void* x, int dtype, int64_t R, int64_t C, int 
                             uint8_t* scales, cudaStream_t stream);
 cudaError_t launch_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C,
                               int fmt, int out_dtype, void* y, cudaStream_t stream);
+cudaError_t launch_quant_tensor_delayed(const void* x, int dtype, int64_t n, int fmt, uint8_t* q,
+                                        float* history, int hist_len, int32_t* pos,
+                                        float* scale_used, uint32_t* partials, cudaStream_t stream);
 cudaError_t launch_set_state(float* scale, int32_t* tracker, float h_scale, int32_t h_tracker,
                              cudaStream_t stream);
 

@@ -114,7 +114,8 @@ __device__ __forceinline__ uint32_t unscale_chunk(const Chunk ch, float inv) {
 __global__ void __launch_bounds__(kUnscaleThreads)
     unscale_check_update_kernel(const Chunk* __restrict__ chunks, int64_t n_chunks, ListWs* ws,
                                 float* scale, int32_t* tracker, int32_t* found_out,
-                                int64_t* skipped, float growth, float backoff, int32_t interval) {
+                                int64_t* skipped, float growth, float backoff, int32_t interval,
+                                ScalerPolicy pol) {
   // Every CTA reads S before it arrives below; the last CTA to arrive is the
   // only writer, so all CTAs unscale with this step's S.
   const float S = *scale;
@@ -137,16 +138,39 @@ __global__ void __launch_bounds__(kUnscaleThreads)
   const int32_t found = atomicOr(&ws->found, 0) != 0;
   float s = *scale;
   int32_t t = *tracker;
-  if (found) {
-    s = __fmul_rn(s, backoff);
-    t = 0;
-    if (skipped) *skipped += 1;
-  } else {
-    t += 1;
-    if (t >= interval) {
-      s = __fmul_rn(s, growth);
+  if (pol.hyst == nullptr) {  // GradScaler loop
+    if (found) {
+      s = __fmul_rn(s, backoff);
       t = 0;
+      if (skipped) *skipped += 1;
+    } else {
+      t += 1;
+      if (t >= interval) {
+        s = __fmul_rn(s, growth);
+        t = 0;
+      }
     }
+  } else {  // hysteresis policy
+    int32_t h = *pol.hyst;
+    if (found) {
+      if (skipped) *skipped += 1;
+      t = 0;
+      if (h > 1) {
+        h -= 1;
+      } else {
+        s = __fmul_rn(s, backoff);
+        if (s < pol.min_scale) s = pol.min_scale;
+      }
+    } else {
+      t += 1;
+      if (pol.consecutive) h = pol.hysteresis;
+      if (t >= interval) {
+        s = __fmul_rn(s, growth);
+        t = 0;
+        if (!pol.consecutive) h = pol.hysteresis;
+      }
+    }
+    *pol.hyst = h;
   }
   *scale = s;
   *tracker = t;
@@ -158,12 +182,13 @@ __global__ void __launch_bounds__(kUnscaleThreads)
 cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks, ListWs* ws,
                                         float* scale, int32_t* tracker, int32_t* found,
                                         int64_t* skipped, float growth, float backoff,
-                                        int32_t interval, cudaStream_t stream) {
+                                        int32_t interval, cudaStream_t stream,
+                                        ScalerPolicy policy) {
   int64_t grid = (int64_t)sm_count() * kUnscaleCtasPerSm;
   if (grid > n_chunks) grid = n_chunks;
   if (grid < 1) grid = 1;
   unscale_check_update_kernel<<<(unsigned)grid, kUnscaleThreads, 0, stream>>>(
-      d_chunks, n_chunks, ws, scale, tracker, found, skipped, growth, backoff, interval);
+      d_chunks, n_chunks, ws, scale, tracker, found, skipped, growth, backoff, interval, policy);
   return cudaGetLastError();
 }
 

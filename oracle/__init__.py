@@ -18,7 +18,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SOURCES = ["fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c"]
+_SOURCES = ["fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c", "delayed.c"]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,11 @@ def _load():
             "orc_amax": (ctypes.c_float, [vp, ctypes.c_int, i64]),
             "orc_scale_from_amax": (ctypes.c_float, [ctypes.c_float, ctypes.c_int]),
             "orc_quant_one": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_float, ctypes.c_int]),
+            "orc_quant_tensor_delayed": (None, [vp, ctypes.c_int, i64, ctypes.c_int, vp, i32,
+                                                ctypes.POINTER(i32), vp, f32p]),
+            "orc_scaler_update_hysteresis": (None, [f32p, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                                    ctypes.POINTER(i64), i32, ctypes.c_float,
+                                                    ctypes.c_float, i32, i32, i32, ctypes.c_float]),
             "orc_e8m0_decode": (ctypes.c_double, [ctypes.c_uint8]),
             "orc_mx_scale_code": (i32, [ctypes.c_double, ctypes.c_int]),
             "orc_quant_mx": (None, [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp]),
@@ -279,3 +284,43 @@ def dequant_mx(q: np.ndarray, scales: np.ndarray, fmt: int, out_dtype: int = F32
     y = np.empty((R, C), np.float32 if out_dtype == F32 else np.uint16)
     _load().orc_dequant_mx(_ptr(q), _ptr(scales), R, C, fmt, out_dtype, _ptr(y))
     return y
+
+
+# ---- delayed scaling and the hysteresis policy ------------------------------
+
+class DelayedScaling:
+    """An amax history of length H (ring buffer) and its write position."""
+
+    def __init__(self, hist_len: int, history=None, pos: int = 0):
+        self.history = np.zeros(hist_len, np.float32) if history is None else \
+            np.array(history, np.float32)
+        self.pos = ctypes.c_int32(pos)
+
+    def quant(self, x: np.ndarray, fmt: int, dtype: int | None = None):
+        """Quantise with the scale from the history, then record x's amax.
+        Returns (codes, scale used)."""
+        x = np.ascontiguousarray(x)
+        code = _dtype_code(x, dtype)
+        q = np.empty(x.shape, np.uint8)
+        s = ctypes.c_float()
+        _load().orc_quant_tensor_delayed(_ptr(x), code, x.size, fmt, _ptr(self.history),
+                                         self.history.size, ctypes.byref(self.pos), _ptr(q),
+                                         ctypes.byref(s))
+        return q, s.value
+
+
+class HysteresisScaler:
+    """S, window tracker, remaining hysteresis and skipped count."""
+
+    def __init__(self, scale: float, hysteresis: int, tracker: int = 0, skipped: int = 0):
+        self.scale = ctypes.c_float(scale)
+        self.tracker = ctypes.c_int32(tracker)
+        self.hyst = ctypes.c_int32(hysteresis)
+        self.skipped = ctypes.c_int64(skipped)
+
+    def update(self, found: int, growth_factor: float, backoff_factor: float, window: int,
+               hysteresis: int, consecutive: bool, min_scale: float) -> None:
+        _load().orc_scaler_update_hysteresis(ctypes.byref(self.scale), ctypes.byref(self.tracker),
+                                             ctypes.byref(self.hyst), ctypes.byref(self.skipped),
+                                             int(found), growth_factor, backoff_factor, window,
+                                             hysteresis, int(consecutive), min_scale)

@@ -94,6 +94,15 @@ void orc_quant_mx(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8
 void orc_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C, int fmt,
                     int out_dtype, void* y);
 
+/* ---- delayed per-tensor scaling and a hysteresis loss-scale policy
+ *      ([P4] "Failure 1"; [P3] DeepSpeed paragraph; see delayed.c) ------- */
+void orc_quant_tensor_delayed(const void* x, int dtype, int64_t n, int fmt, float* history,
+                              int32_t hist_len, int32_t* pos, uint8_t* q, float* scale_used);
+void orc_scaler_update_hysteresis(float* scale, int32_t* tracker, int32_t* hyst, int64_t* skipped,
+                                  int32_t found, float growth_factor, float backoff_factor,
+                                  int32_t window, int32_t hysteresis, int32_t consecutive,
+                                  float min_scale);
+
 /* Pieces of the block path, exposed so tests can pin each step. */
 float orc_amax(const void* x, int dtype, int64_t n);          /* NaN-propagating */
 float orc_scale_from_amax(float amax, int fmt);               /* max(a,1e-12)/MAX */

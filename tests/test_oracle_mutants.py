@@ -16,7 +16,7 @@ from conftest import ROOT
 
 ORACLE = os.path.join(ROOT, "oracle")
 PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_scaler.py", "tests/test_oracle_quant.py",
-        "tests/test_oracle_mx.py"]
+        "tests/test_oracle_mx.py", "tests/test_oracle_delayed.py"]
 
 MUTANTS = {
     "ties round up instead of to even": (
@@ -49,6 +49,15 @@ MUTANTS = {
     "MX scale applied the wrong way": (
         "mx_quant.c", "ldexp(orc__load_elem(x, dtype, base + i), 127 - code)",
         "ldexp(orc__load_elem(x, dtype, base + i), code - 127)"),
+    "delayed scale from the current amax": (
+        "delayed.c", "float s = orc_scale_from_amax(hnan ? NAN : hmax, fmt);",
+        "float s = orc_scale_from_amax(orc_amax(x, dtype, n), fmt);"),
+    "history position not advanced": (
+        "delayed.c", "*pos = (*pos + 1) % hist_len;", ""),
+    "hysteresis not restored on growth": (
+        "delayed.c", "    if (!consecutive) *hyst = hysteresis;\n", ""),
+    "min loss scale ignored": (
+        "delayed.c", "*scale = s < min_scale ? min_scale : s;", "*scale = s;"),
     "dequant scale index transposed": (
         "fp8_quant.c", "float s = scales[(r / br) * nbc + c / bc];", "float s = scales[(c / bc) * (R / br) + r / br];"),
 }
@@ -57,7 +66,7 @@ MUTANTS = {
 def _build_variant(tmp, name, patch):
     d = os.path.join(tmp, name.replace(" ", "_").replace("(", "").replace(")", "").replace(",", ""))
     os.makedirs(d)
-    for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c"]:
+    for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c", "delayed.c"]:
         shutil.copy(os.path.join(ORACLE, f), d)
     if patch is not None:
         fname, old, new = patch
@@ -69,15 +78,26 @@ def _build_variant(tmp, name, patch):
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
                     "-shared", "-o", lib, *[os.path.join(d, f) for f in
                                             ["fp_formats.c", "gradscaler.c", "fp8_quant.c",
-                                             "mx_quant.c"]], "-lm"],
+                                             "mx_quant.c", "delayed.c"]], "-lm"],
                    check=True)
     return lib
 
 
-def _run_pins(lib):
+# The pin files that exercise each source file (a planted mistake runs only
+# these; the unmodified build runs them all).
+PINS_FOR = {
+    "fp_formats.c": ["tests/test_oracle_formats.py", "tests/test_oracle_quant.py", "tests/test_oracle_mx.py"],
+    "gradscaler.c": ["tests/test_oracle_scaler.py", "tests/test_oracle_formats.py"],
+    "fp8_quant.c": ["tests/test_oracle_quant.py", "tests/test_oracle_delayed.py"],
+    "mx_quant.c": ["tests/test_oracle_mx.py"],
+    "delayed.c": ["tests/test_oracle_delayed.py"],
+}
+
+
+def _run_pins(lib, pins):
     env = dict(os.environ, GS_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "-m", "not gpu", *PINS], cwd=ROOT, env=env, capture_output=True, text=True)
+                        "-m", "not gpu", *pins], cwd=ROOT, env=env, capture_output=True, text=True)
     return r.returncode
 
 
@@ -85,8 +105,9 @@ def test_pins_catch_every_planted_mistake():
     with tempfile.TemporaryDirectory() as tmp:
         cases = {"unmodified": None, **MUTANTS}
         libs = {name: _build_variant(tmp, name, patch) for name, patch in cases.items()}
+        pins = {name: PINS if patch is None else PINS_FOR[patch[0]] for name, patch in cases.items()}
         with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-            rc = dict(zip(libs, ex.map(_run_pins, libs.values())))
+            rc = dict(zip(libs, ex.map(_run_pins, libs.values(), [pins[n] for n in libs])))
     assert rc.pop("unmodified") == 0, "the pins must pass on the unmodified oracle"
     survived = [name for name, code in rc.items() if code == 0]
     assert not survived, f"mistakes no pin caught: {survived}"
