@@ -60,7 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--only", choices=["unscale", "quant_1x128", "dequant", "quant_128x128",
-                                      "quant_tensor", "quant_mx", "dequant_mx", "quant_delayed"],
+                                      "quant_tensor", "quant_mx", "dequant_mx", "quant_delayed",
+                                      "unscale_norm", "master_update"],
                    help="time one kernel alone on a small case (for ncu captures)")
     return p.parse_args(argv)
 
@@ -541,7 +542,30 @@ def run_only(args):
     torch.cuda.set_device(0)
     st = torch.cuda.current_stream().cuda_stream
     dev = "cuda"
-    if args.only == "unscale":
+    if args.only in ("unscale_norm", "master_update"):
+        cfg = wl.cfg2_grads()
+        n_t = 18
+        grads = [torch.empty(n, dtype=torch.float16, device=dev) for n in cfg.numels[:n_t]]
+        outs = [torch.empty(n, dtype=torch.float32, device=dev) for n in cfg.numels[:n_t]]
+        for t, g in enumerate(grads):
+            dg.fill_device(cfg.spec(t, 0), 0, g.numel(), g.data_ptr(), st)
+        tl = gs.gs_tensor_list_create(grads, outs)
+        sc = torch.tensor([65536.0], device=dev)
+        tr = torch.zeros(1, dtype=torch.int32, device=dev)
+        fi = torch.zeros(1, dtype=torch.int32, device=dev)
+        nrm = torch.empty(1, dtype=torch.float32, device=dev)
+        gs.gs_unscale_check_update_norm(tl, sc, tr, fi, nrm, None, 2.0, 0.5, 2000)
+        n_par = sum(cfg.numels[:n_t])
+        if args.only == "unscale_norm":
+            fn = lambda: gs.gs_unscale_check_update_norm(tl, sc, tr, fi, nrm, None, 2.0, 0.5, 2000)
+            nbytes = 6 * n_par
+        else:
+            w32 = [torch.zeros(n, dtype=torch.float32, device=dev) for n in cfg.numels[:n_t]]
+            wbf = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for n in cfg.numels[:n_t]]
+            pl = gs.gs_param_list_create(w32, outs, wbf)
+            fn = lambda: gs.gs_master_update_sgd(pl, 1e-4, 1.0, nrm, fi)
+            nbytes = 14 * n_par
+    elif args.only == "unscale":
         cfg = wl.cfg2_grads()
         n_t = 18
         grads = [torch.empty(n, dtype=torch.float16, device=dev) for n in cfg.numels[:n_t]]

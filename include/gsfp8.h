@@ -120,6 +120,19 @@ int gs_unscale_check_update(const gs_tensor_list* list, float* scale, int32_t* g
                             int32_t* found_inf, int64_t* skipped, float growth_factor,
                             float backoff_factor, int32_t growth_interval, void* stream);
 
+/* The same step, also returning the global L2 norm of the unscaled
+ * gradients (step 5 of [P3]'s training step clips by it):
+ *   *grad_norm = sqrt(sum over every element of out_i^2)  (device fp32)
+ * computed in the same pass (no extra traffic): fp32 fused multiply-adds
+ * within a chunk of at most 32 terms per thread, compensated fp32 sums
+ * across chunks, fp64 beyond; the sum of squares has a relative error below
+ * 35 * 2^-24 and is bitwise reproducible on one device.  A step with
+ * Inf/NaN gives an Inf/NaN norm. */
+int gs_unscale_check_update_norm(const gs_tensor_list* list, float* scale, int32_t* growth_tracker,
+                                 int32_t* found_inf, int64_t* skipped, float growth_factor,
+                                 float backoff_factor, int32_t growth_interval, float* grad_norm,
+                                 void* stream);
+
 /* The same step under a loss-scale policy with hysteresis ([P3] DeepSpeed
  * paragraph: loss_scale_window 1000, hysteresis 2, consecutive_hysteresis
  * false, min_loss_scale 1 -- the pages name the settings; this reading is
@@ -138,6 +151,35 @@ int gs_unscale_check_update_hysteresis(const gs_tensor_list* list, float* scale,
                                        float backoff_factor, int32_t window, int32_t hysteresis,
                                        int32_t consecutive_hysteresis, float min_scale,
                                        void* stream);
+
+/* ------------------------------------------------------------------------
+ * The consumer of the step ([P3] six-step training step, step 5: clip and
+ * update -- apply guardrails, write into FP32 master state, and skip
+ * invalid steps; [P5] "Range and precision": FP32 master weights converted
+ * to bf16 each step for the forward pass).
+ * --------------------------------------------------------------------- */
+
+/* Opaque list of parameters: per tensor, its fp32 master weights (updated
+ * in place), an optional bf16 copy (master_bf16 NULL or master_bf16[i]
+ * NULL: none) and its fp32 gradients (typically the outs of a
+ * gs_tensor_list).  Allocates a device chunk table (synchronous). */
+typedef struct gs_param_list gs_param_list;
+int gs_param_list_create(float* const* master, uint16_t* const* master_bf16,
+                         const float* const* grads, const int64_t* numels, int32_t n_tensors,
+                         gs_param_list** out);
+int gs_param_list_destroy(gs_param_list* list);
+
+/* SGD step on every parameter of the list, one launch:
+ *   if *found_inf != 0 (device): nothing is written (the skipped step);
+ *   coef = max_norm / *grad_norm if max_norm > 0 and *grad_norm > max_norm,
+ *          else 1 (fp32 division);
+ *   w = w - lr * (coef * g), each product and the difference rounded to
+ *       fp32 separately; bf16 copy = w rounded to nearest even.
+ * grad_norm: device fp32 (from gs_unscale_check_update_norm); may be NULL
+ * when max_norm <= 0 (no clipping).  Stream-ordered after the step that
+ * produced found_inf / grad_norm; nothing is read on the host. */
+int gs_master_update_sgd(const gs_param_list* list, float lr, float max_norm,
+                         const float* grad_norm, const int32_t* found_inf, void* stream);
 
 /* Checkpoint support: the scaler's whole state is {S, growth_tracker}.
  * get: copies the two device scalars to host variables and waits for the

@@ -22,6 +22,7 @@ __all__ = [
     "fp8_dequant", "gs_ws_bytes", "gs_device_status", "lib_path",
     "gs_unscale_check_update_noalloc", "gs_noalloc_limits", "fp8_quant_mx", "fp8_dequant_mx",
     "gs_unscale_check_update_hysteresis", "fp8_quant_tensor_delayed",
+    "gs_unscale_check_update_norm", "ParamList", "gs_param_list_create", "gs_master_update_sgd",
 ]
 
 GS_OK, GS_ERR_NULL, GS_ERR_SHAPE, GS_ERR_DTYPE, GS_ERR_ARG, GS_ERR_CUDA, GS_ERR_TIMEOUT = range(7)
@@ -60,6 +61,10 @@ def _load_lib() -> ctypes.CDLL:
         "fp8_quant_tensor": (ci, [vp, ci, i64, ci, vp, vp, vp, vp]),
         "fp8_dequant": (ci, [vp, vp, i64, i64, i32, i32, ci, ci, vp, vp]),
         "gs_device_status": (ci, [ctypes.POINTER(i32), vp]),
+        "gs_unscale_check_update_norm": (ci, [vp, vp, vp, vp, vp, f32, f32, i32, vp, vp]),
+        "gs_param_list_create": (ci, [vp, vp, vp, vp, i32, ctypes.POINTER(vp)]),
+        "gs_param_list_destroy": (ci, [vp]),
+        "gs_master_update_sgd": (ci, [vp, f32, f32, vp, vp, vp]),
         "gs_unscale_check_update_hysteresis": (ci, [vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32,
                                                     f32, vp]),
         "fp8_quant_tensor_delayed": (ci, [vp, ci, i64, ci, vp, vp, i32, vp, vp, vp, vp]),
@@ -204,6 +209,67 @@ def gs_noalloc_limits() -> tuple[int, int, int]:
     _check(_lib.gs_noalloc_limits(ctypes.byref(t), ctypes.byref(c), ctypes.byref(e)),
            "gs_noalloc_limits")
     return t.value, c.value, e.value
+
+
+def gs_unscale_check_update_norm(tlist: TensorList, scale: torch.Tensor,
+                                 growth_tracker: torch.Tensor, found_inf: torch.Tensor,
+                                 grad_norm: torch.Tensor, skipped: torch.Tensor | None = None,
+                                 growth_factor: float = 2.0, backoff_factor: float = 0.5,
+                                 growth_interval: int = 2000, stream=None) -> None:
+    _check(_lib.gs_unscale_check_update_norm(tlist.handle, _ptr(scale), _ptr(growth_tracker),
+                                             _ptr(found_inf), _ptr(skipped), growth_factor,
+                                             backoff_factor, growth_interval, _ptr(grad_norm),
+                                             _stream(stream)), "gs_unscale_check_update_norm")
+
+
+class ParamList:
+    """Owns a ``gs_param_list`` handle: fp32 master weights, optional bf16
+    copies and fp32 gradients, tensor by tensor."""
+
+    def __init__(self, master: list[torch.Tensor], grads: list[torch.Tensor],
+                 master_bf16: list[torch.Tensor] | None = None):
+        n = len(master)
+        if len(grads) != n or (master_bf16 is not None and len(master_bf16) != n):
+            raise ValueError("lists differ in length")
+        for i in range(n):
+            _contig(master[i], "master")
+            _contig(grads[i], "grad")
+            if master[i].dtype != torch.float32 or grads[i].dtype != torch.float32 or \
+                    master[i].numel() != grads[i].numel():
+                raise ValueError("master and grads must be float32 of equal numel")
+            if master_bf16 is not None and (master_bf16[i].dtype != torch.bfloat16 or
+                                            master_bf16[i].numel() != master[i].numel()):
+                raise ValueError("master_bf16 must be bfloat16 of the same numel")
+        self._keep = (list(master), list(grads), list(master_bf16 or []))
+        k = max(n, 1)
+        mp = (ctypes.c_void_p * k)(*[t.data_ptr() for t in master])
+        gp = (ctypes.c_void_p * k)(*[t.data_ptr() for t in grads])
+        bp = (ctypes.c_void_p * k)(*[t.data_ptr() for t in master_bf16]) if master_bf16 else None
+        ne = (ctypes.c_int64 * k)(*[t.numel() for t in master])
+        h = ctypes.c_void_p()
+        _check(_lib.gs_param_list_create(mp, bp, gp, ne, n, ctypes.byref(h)), "gs_param_list_create")
+        self.handle = h
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            _lib.gs_param_list_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def gs_param_list_create(master, grads, master_bf16=None) -> ParamList:
+    return ParamList(master, grads, master_bf16)
+
+
+def gs_master_update_sgd(plist: ParamList, lr: float, max_norm: float, grad_norm: torch.Tensor | None,
+                         found_inf: torch.Tensor, stream=None) -> None:
+    _check(_lib.gs_master_update_sgd(plist.handle, lr, max_norm, _ptr(grad_norm), _ptr(found_inf),
+                                     _stream(stream)), "gs_master_update_sgd")
 
 
 def gs_unscale_check_update_hysteresis(tlist: TensorList, scale: torch.Tensor,

@@ -21,7 +21,15 @@ struct gs_tensor_list {
   gs::Chunk* d_chunks;
   int64_t n_chunks;
   int64_t total;
-  gs::ListWs* d_ws;
+  gs::ListWs* d_ws;       // epilogue words, then the norm slots
+  double* d_norm_slots;   // one per CTA of the unscale grid
+};
+
+struct gs_param_list {
+  int device;
+  gs::MChunk* d_chunks;
+  int64_t n_chunks;
+  int64_t total;
 };
 
 namespace gs {
@@ -146,10 +154,13 @@ int gs_tensor_list_create(const void* const* grads, void* const* outs, const int
       chunks.push_back(Chunk{g + off, o + off, (n - off) < kChunkElems ? (n - off) : kChunkElems});
     total += n;
   }
-  gs_tensor_list* l = new (std::nothrow) gs_tensor_list{current_device(), nullptr, 0, total, nullptr};
+  gs_tensor_list* l =
+      new (std::nothrow) gs_tensor_list{current_device(), nullptr, 0, total, nullptr, nullptr};
   if (!l) return GS_ERR_ARG;
-  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&l->d_ws), sizeof(ListWs));
-  if (e == cudaSuccess) e = cudaMemset(l->d_ws, 0, sizeof(ListWs));
+  const size_t ws_bytes = 256 + (size_t)sm_count() * kUnscaleCtasPerSm * sizeof(double);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&l->d_ws), ws_bytes);
+  if (e == cudaSuccess) e = cudaMemset(l->d_ws, 0, ws_bytes);
+  l->d_norm_slots = reinterpret_cast<double*>(reinterpret_cast<char*>(l->d_ws) + 256);
   if (e == cudaSuccess && !chunks.empty()) {
     e = cudaMalloc(reinterpret_cast<void**>(&l->d_chunks), chunks.size() * sizeof(Chunk));
     if (e == cudaSuccess)
@@ -205,6 +216,98 @@ int gs_unscale_check_update(const gs_tensor_list* list, float* scale, int32_t* g
                                               growth_tracker, found_inf, skipped, growth_factor,
                                               backoff_factor, growth_interval,
                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_unscale_check_update_norm(const gs_tensor_list* list, float* scale, int32_t* growth_tracker,
+                                 int32_t* found_inf, int64_t* skipped, float growth_factor,
+                                 float backoff_factor, int32_t growth_interval, float* grad_norm,
+                                 void* stream) {
+  if (!list || !scale || !growth_tracker || !found_inf || !grad_norm) return GS_ERR_NULL;
+  if (growth_interval < 1) return GS_ERR_ARG;
+  if (!std::isfinite(growth_factor) || !(growth_factor > 0.0f) || !std::isfinite(backoff_factor) ||
+      !(backoff_factor > 0.0f))
+    return GS_ERR_ARG;
+  if (list->device != current_device()) return GS_ERR_ARG;
+  if (!aligned(scale, 4) || !aligned(growth_tracker, 4) || !aligned(found_inf, 4) ||
+      !aligned(grad_norm, 4) || (skipped && !aligned(skipped, 8)))
+    return GS_ERR_ARG;
+  if (!device_reachable(scale) || !device_reachable(growth_tracker) || !device_reachable(found_inf) ||
+      !device_reachable(grad_norm) || (skipped && !device_reachable(skipped)))
+    return GS_ERR_ARG;
+  cudaError_t e = launch_unscale_check_update(
+      list->d_chunks, list->n_chunks, list->d_ws, scale, growth_tracker, found_inf, skipped,
+      growth_factor, backoff_factor, growth_interval, static_cast<cudaStream_t>(stream),
+      ScalerPolicy{nullptr, 1, 0, 0.0f}, grad_norm, list->d_norm_slots);
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_param_list_create(float* const* master, uint16_t* const* master_bf16,
+                         const float* const* grads, const int64_t* numels, int32_t n_tensors,
+                         gs_param_list** out) {
+  if (!out) return GS_ERR_NULL;
+  *out = nullptr;
+  if (n_tensors < 0) return GS_ERR_SHAPE;
+  if (n_tensors > 0 && (!master || !grads || !numels)) return GS_ERR_NULL;
+  std::vector<MChunk> chunks;
+  int64_t total = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t n = numels[i];
+    if (n < 0 || n > (INT64_MAX >> 3)) return GS_ERR_SHAPE;
+    if (n == 0) continue;
+    uint16_t* wb = master_bf16 ? master_bf16[i] : nullptr;
+    if (!master[i] || !grads[i]) return GS_ERR_NULL;
+    if (!aligned(master[i], 4) || !aligned(grads[i], 4) || (wb && !aligned(wb, 2))) return GS_ERR_ARG;
+    if (!device_reachable(master[i]) || !device_reachable(grads[i]) || (wb && !device_reachable(wb)))
+      return GS_ERR_ARG;
+    if (overlaps(master[i], (size_t)n * 4, grads[i], (size_t)n * 4) ||
+        (wb && (overlaps(wb, (size_t)n * 2, master[i], (size_t)n * 4) ||
+                overlaps(wb, (size_t)n * 2, grads[i], (size_t)n * 4))))
+      return GS_ERR_ARG;
+    for (int64_t off = 0; off < n; off += kChunkElems)
+      chunks.push_back(MChunk{master[i] + off, wb ? wb + off : nullptr, grads[i] + off,
+                              (n - off) < kChunkElems ? (n - off) : kChunkElems});
+    total += n;
+  }
+  gs_param_list* l = new (std::nothrow) gs_param_list{current_device(), nullptr, 0, total};
+  if (!l) return GS_ERR_ARG;
+  cudaError_t e = cudaSuccess;
+  if (!chunks.empty()) {
+    e = cudaMalloc(reinterpret_cast<void**>(&l->d_chunks), chunks.size() * sizeof(MChunk));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(l->d_chunks, chunks.data(), chunks.size() * sizeof(MChunk),
+                     cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    if (l->d_chunks) cudaFree(l->d_chunks);
+    delete l;
+    return cuda_fail(e);
+  }
+  l->n_chunks = (int64_t)chunks.size();
+  *out = l;
+  return GS_OK;
+}
+
+int gs_param_list_destroy(gs_param_list* list) {
+  if (!list) return GS_OK;
+  int prev = current_device();
+  cudaSetDevice(list->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (list->d_chunks) cudaFree(list->d_chunks);
+  cudaSetDevice(prev);
+  delete list;
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_master_update_sgd(const gs_param_list* list, float lr, float max_norm,
+                         const float* grad_norm, const int32_t* found_inf, void* stream) {
+  if (!list || !found_inf || (max_norm > 0.0f && !grad_norm)) return GS_ERR_NULL;
+  if (!std::isfinite(lr) || !std::isfinite(max_norm)) return GS_ERR_ARG;
+  if (list->device != current_device()) return GS_ERR_ARG;
+  if (!aligned(found_inf, 4) || (grad_norm && !aligned(grad_norm, 4))) return GS_ERR_ARG;
+  if (!device_reachable(found_inf) || (grad_norm && !device_reachable(grad_norm))) return GS_ERR_ARG;
+  cudaError_t e = launch_master_update_sgd(list->d_chunks, list->n_chunks, lr, max_norm,
+                                           grad_norm, found_inf, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
 

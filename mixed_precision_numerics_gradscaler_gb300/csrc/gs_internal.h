@@ -20,11 +20,22 @@ struct Chunk {
 constexpr int64_t kChunkElems = 8192;
 
 // Per-list device workspace of the last-CTA epilogue.  Both words return
-// to zero at the end of every call.
+// to zero at the end of every call.  A list created by
+// gs_tensor_list_create is followed by kUnscaleMaxCtas double slots for the
+// per-CTA sums of squares of the norm-computing form.
 struct ListWs {
   unsigned int arrived;
   int32_t found;
   int32_t pad[2];
+};
+constexpr int kUnscaleCtasPerSm = 32;
+
+// One contiguous run of a parameter tensor for the master-weight update.
+struct MChunk {
+  float* w;            // fp32 master weights (updated in place)
+  uint16_t* w_bf16;    // bf16 copy for the forward pass, or nullptr
+  const float* g;      // unscaled fp32 gradients
+  int64_t n;
 };
 
 // Loss-scale policy applied by the last CTA of the unscale kernel.  With
@@ -51,7 +62,11 @@ cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks,
                                         float* scale, int32_t* tracker, int32_t* found,
                                         int64_t* skipped, float growth, float backoff,
                                         int32_t interval, cudaStream_t stream,
-                                        ScalerPolicy policy = ScalerPolicy{nullptr, 1, 0, 0.0f});
+                                        ScalerPolicy policy = ScalerPolicy{nullptr, 1, 0, 0.0f},
+                                        float* grad_norm = nullptr, double* norm_slots = nullptr);
+cudaError_t launch_master_update_sgd(const MChunk* d_chunks, int64_t n_chunks, float lr,
+                                     float max_norm, const float* grad_norm,
+                                     const int32_t* found_inf, cudaStream_t stream);
 
 cudaError_t launch_quant_1x128(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
                                float* scales, cudaStream_t stream);

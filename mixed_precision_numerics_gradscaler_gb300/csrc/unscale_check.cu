@@ -7,6 +7,8 @@
 //   out = fp32(g) * fp32(1/S) for every element of every tensor,
 //   found_inf = any scaled FP16 input with an all-ones exponent field,
 //   then S / growth tracker updated on the device by the last CTA to finish.
+// Optionally (step 5's clipping needs it) the same pass returns the global
+// L2 norm of the unscaled gradients.
 //
 // Layout: an oversubscribed grid (32 CTAs per SM, four or more waves of
 // resident CTAs) walks the list's chunk table grid-stride.  A full 8192-
@@ -26,7 +28,6 @@ namespace gs {
 
 constexpr int kUnscaleThreads = 256;
 constexpr int kUnscaleUnroll = 4;
-constexpr int kUnscaleCtasPerSm = 32;
 static_assert(kChunkElems == 2 * 16 * kUnscaleThreads, "one pass of v8 pairs per chunk");
 
 // 0xFFFF in each 16-bit lane whose exponent field is all ones (Inf / NaN).
@@ -34,57 +35,44 @@ __device__ __forceinline__ uint32_t nonfinite2(uint32_t w) {
   return __vcmpeq2(w & 0x7C007C00u, 0x7C007C00u);
 }
 
-__device__ __forceinline__ void unscale8(uint4 v, float inv, uint4* out, uint32_t& bad) {
+// Sum of squares of the unscaled values, accumulated in fp32 within a
+// chunk (at most 32 terms per thread), only in the NORM form.
+template <bool NORM>
+__device__ __forceinline__ void sq_acc(float& acc, float v) {
+  if constexpr (NORM) acc = __fmaf_rn(v, v, acc);
+}
+
+template <bool NORM>
+__device__ __forceinline__ void unscale8(uint4 v, float inv, uint4* out, uint32_t& bad, float& acc) {
   bad |= nonfinite2(v.x) | nonfinite2(v.y) | nonfinite2(v.z) | nonfinite2(v.w);
-  uint4 a, b;
-  a.x = __float_as_uint(__fmul_rn(lo_f16(v.x), inv));
-  a.y = __float_as_uint(__fmul_rn(hi_f16(v.x), inv));
-  a.z = __float_as_uint(__fmul_rn(lo_f16(v.y), inv));
-  a.w = __float_as_uint(__fmul_rn(hi_f16(v.y), inv));
-  b.x = __float_as_uint(__fmul_rn(lo_f16(v.z), inv));
-  b.y = __float_as_uint(__fmul_rn(hi_f16(v.z), inv));
-  b.z = __float_as_uint(__fmul_rn(lo_f16(v.w), inv));
-  b.w = __float_as_uint(__fmul_rn(hi_f16(v.w), inv));
-  st_stream(out, a);
-  st_stream(out + 1, b);
-}
-
-__device__ __forceinline__ void unscale1(const uint16_t* in, float* out, int64_t i, float inv,
-                                         uint32_t& bad) {
-  const uint32_t h = in[i];
-  bad |= ((h & 0x7C00u) == 0x7C00u);
-  out[i] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), inv);
-}
-
-// 16 FP16 -> 16 FP32 (two 32-byte stores).
-__device__ __forceinline__ void unscale16(const V8& v, float inv, uint8_t* out, uint32_t& bad) {
-  V8 a, b;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    bad |= nonfinite2(v.w[j]) | nonfinite2(v.w[j + 4]);
-    a.w[2 * j] = __float_as_uint(__fmul_rn(lo_f16(v.w[j]), inv));
-    a.w[2 * j + 1] = __float_as_uint(__fmul_rn(hi_f16(v.w[j]), inv));
-    b.w[2 * j] = __float_as_uint(__fmul_rn(lo_f16(v.w[j + 4]), inv));
-    b.w[2 * j + 1] = __float_as_uint(__fmul_rn(hi_f16(v.w[j + 4]), inv));
+    f[2 * j] = __fmul_rn(lo_f16(w[j]), inv);
+    f[2 * j + 1] = __fmul_rn(hi_f16(w[j]), inv);
+    sq_acc<NORM>(acc, f[2 * j]);
+    sq_acc<NORM>(acc, f[2 * j + 1]);
   }
-  st_stream8(out, a);
-  st_stream8(out + 32, b);
+  st_stream(out, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                            __float_as_uint(f[3])));
+  st_stream(out + 1, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
+                                __float_as_uint(f[6]), __float_as_uint(f[7])));
 }
 
-// Full, 32-byte-aligned chunk: two loads in flight per thread, then stores.
-__device__ __forceinline__ uint32_t unscale_chunk_full(const Chunk ch, float inv) {
-  const uint8_t* in = reinterpret_cast<const uint8_t*>(ch.in);
-  uint8_t* out = reinterpret_cast<uint8_t*>(ch.out);
-  const int v0 = threadIdx.x, v1 = threadIdx.x + kUnscaleThreads;
-  const V8 a = ld_stream8(in + 32 * v0);
-  const V8 b = ld_stream8(in + 32 * v1);
-  uint32_t bad = 0;
-  unscale16(a, inv, out + 64 * v0, bad);
-  unscale16(b, inv, out + 64 * v1, bad);
-  return bad;
+template <bool NORM>
+__device__ __forceinline__ void unscale1(const uint16_t* in, float* out, int64_t i, float inv,
+                                         uint32_t& bad, float& acc) {
+  const uint32_t h = in[i];
+  bad |= ((h & 0x7C00u) == 0x7C00u);
+  const float f = __fmul_rn(__half2float(__ushort_as_half((unsigned short)h)), inv);
+  sq_acc<NORM>(acc, f);
+  out[i] = f;
 }
 
-__device__ __forceinline__ uint32_t unscale_chunk(const Chunk ch, float inv) {
+// Any chunk: 16-byte vectors between a scalar head and tail.
+template <bool NORM>
+__device__ __forceinline__ uint32_t unscale_chunk(const Chunk ch, float inv, float& acc) {
   const uint16_t* in = ch.in;
   float* out = ch.out;
   const int64_t n = ch.n;
@@ -94,7 +82,7 @@ __device__ __forceinline__ uint32_t unscale_chunk(const Chunk ch, float inv) {
   int64_t head = (int64_t)(((16u - ((uint32_t)(uintptr_t)in & 15u)) & 15u) >> 1);
   if (head > n) head = n;
   if ((((uintptr_t)(out + head)) & 15u) != 0) head = n;
-  for (int64_t i = threadIdx.x; i < head; i += blockDim.x) unscale1(in, out, i, inv, bad);
+  for (int64_t i = threadIdx.x; i < head; i += blockDim.x) unscale1<NORM>(in, out, i, inv, bad, acc);
   const int64_t nv = (n - head) >> 3;
   const uint4* in8 = reinterpret_cast<const uint4*>(in + head);
   uint4* out4 = reinterpret_cast<uint4*>(out + head);
@@ -104,37 +92,136 @@ __device__ __forceinline__ uint32_t unscale_chunk(const Chunk ch, float inv) {
 #pragma unroll
     for (int u = 0; u < kUnscaleUnroll; ++u) r[u] = ld_stream(in8 + v + u * blockDim.x);
 #pragma unroll
-    for (int u = 0; u < kUnscaleUnroll; ++u) unscale8(r[u], inv, out4 + 2 * (v + u * blockDim.x), bad);
+    for (int u = 0; u < kUnscaleUnroll; ++u)
+      unscale8<NORM>(r[u], inv, out4 + 2 * (v + u * blockDim.x), bad, acc);
   }
-  for (; v < nv; v += blockDim.x) unscale8(ld_stream(in8 + v), inv, out4 + 2 * v, bad);
-  for (int64_t i = head + nv * 8 + threadIdx.x; i < n; i += blockDim.x) unscale1(in, out, i, inv, bad);
+  for (; v < nv; v += blockDim.x) unscale8<NORM>(ld_stream(in8 + v), inv, out4 + 2 * v, bad, acc);
+  for (int64_t i = head + nv * 8 + threadIdx.x; i < n; i += blockDim.x)
+    unscale1<NORM>(in, out, i, inv, bad, acc);
   return bad;
 }
 
+// 16 FP16 -> 16 FP32 (two 32-byte stores).
+template <bool NORM>
+__device__ __forceinline__ void unscale16(const V8& v, float inv, uint8_t* out, uint32_t& bad,
+                                          float& acc) {
+  V8 a, b;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    bad |= nonfinite2(v.w[j]) | nonfinite2(v.w[j + 4]);
+    const float f0 = __fmul_rn(lo_f16(v.w[j]), inv), f1 = __fmul_rn(hi_f16(v.w[j]), inv);
+    const float f2 = __fmul_rn(lo_f16(v.w[j + 4]), inv), f3 = __fmul_rn(hi_f16(v.w[j + 4]), inv);
+    sq_acc<NORM>(acc, f0);
+    sq_acc<NORM>(acc, f1);
+    sq_acc<NORM>(acc, f2);
+    sq_acc<NORM>(acc, f3);
+    a.w[2 * j] = __float_as_uint(f0);
+    a.w[2 * j + 1] = __float_as_uint(f1);
+    b.w[2 * j] = __float_as_uint(f2);
+    b.w[2 * j + 1] = __float_as_uint(f3);
+  }
+  st_stream8(out, a);
+  st_stream8(out + 32, b);
+}
+
+// Full, 32-byte-aligned chunk: two loads in flight per thread, then stores.
+template <bool NORM>
+__device__ __forceinline__ uint32_t unscale_chunk_full(const Chunk ch, float inv, float& acc) {
+  const uint8_t* in = reinterpret_cast<const uint8_t*>(ch.in);
+  uint8_t* out = reinterpret_cast<uint8_t*>(ch.out);
+  const int v0 = threadIdx.x, v1 = threadIdx.x + kUnscaleThreads;
+  const V8 a = ld_stream8(in + 32 * v0);
+  const V8 b = ld_stream8(in + 32 * v1);
+  uint32_t bad = 0;
+  unscale16<NORM>(a, inv, out + 64 * v0, bad, acc);
+  unscale16<NORM>(b, inv, out + 64 * v1, bad, acc);
+  return bad;
+}
+
+// With NORM the kernel also returns sqrt(sum of squares) of every unscaled
+// value: fp32 fused multiply-adds within a chunk (at most 32 terms per
+// thread), Kahan-compensated fp32 sums across a thread's chunks (GB300's
+// fp64 rate is far below its fp32 rate, so fp64 stays out of the loop),
+// fp64 from the thread total on: across the CTA, one slot per CTA, and the
+// last CTA adds the slots in a fixed order.  Deterministic for a given grid; the
+// sum of squares carries a relative error below 35 * 2^-24 (all terms are
+// non-negative: 32 u per chunk, 2 u for the compensated sum, the rest in
+// fp64).
+template <bool NORM>
 __global__ void __launch_bounds__(kUnscaleThreads)
     unscale_check_update_kernel(const Chunk* __restrict__ chunks, int64_t n_chunks, ListWs* ws,
                                 float* scale, int32_t* tracker, int32_t* found_out,
                                 int64_t* skipped, float growth, float backoff, int32_t interval,
-                                ScalerPolicy pol) {
+                                ScalerPolicy pol, float* grad_norm, double* norm_slots) {
   // Every CTA reads S before it arrives below; the last CTA to arrive is the
   // only writer, so all CTAs unscale with this step's S.
+  // fp32(1/S) as the oracle defines it, (float)(1.0 / (double)S): for every
+  // fp32 S this is the correctly rounded fp32 reciprocal (checked over all
+  // 2^32 patterns), so no fp64 division is needed.
   const float S = *scale;
-  const float inv = (float)(1.0 / (double)S);
+  const float inv = __frcp_rn(S);
   uint32_t bad = 0;
+  float ksum = 0.0f, kcomp = 0.0f;  // Kahan sum of the chunk sums
   for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
     const Chunk ch = chunks[c];
     const bool full = ch.n == kChunkElems && ((((uintptr_t)ch.in) | ((uintptr_t)ch.out)) & 31u) == 0;
-    bad |= full ? unscale_chunk_full(ch, inv) : unscale_chunk(ch, inv);
+    float acc = 0.0f;
+    bad |= full ? unscale_chunk_full<NORM>(ch, inv, acc) : unscale_chunk<NORM>(ch, inv, acc);
+    if constexpr (NORM) {
+      const float y = __fsub_rn(acc, kcomp);
+      const float t = __fadd_rn(ksum, y);
+      kcomp = __fsub_rn(__fsub_rn(t, ksum), y);
+      ksum = t;
+    }
+  }
+  if constexpr (NORM) {
+    double sumsq = (double)ksum - (double)kcomp;
+    __shared__ double red[kUnscaleThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sumsq += __shfl_xor_sync(0xFFFFFFFFu, sumsq, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sumsq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double t = 0.0;
+      for (int w = 0; w < kUnscaleThreads / 32; ++w) t += red[w];
+      norm_slots[blockIdx.x] = t;
+    }
   }
 
   const int any_bad = __syncthreads_or(bad != 0);
-  if (threadIdx.x != 0) return;
-  if (any_bad) atomicOr(&ws->found, 1);
-  __threadfence();
-  const unsigned int prev = atomicAdd(&ws->arrived, 1u);
-  if (prev != gridDim.x - 1) return;
-  // Last CTA: every flag is in; apply the control loop.
-  __threadfence();
+  double norm_total = 0.0;
+  if constexpr (NORM) {
+    // The whole last CTA adds the slots (one fp64 add chain per thread over
+    // a fixed stride, then a fixed-order tree): a serial chain of dependent
+    // fp64 adds in one thread would take longer than the pass itself.
+    __shared__ int last;
+    __shared__ double red2[kUnscaleThreads / 32];
+    if (threadIdx.x == 0) {
+      if (any_bad) atomicOr(&ws->found, 1);
+      __threadfence();
+      last = atomicAdd(&ws->arrived, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double t = 0.0;
+    for (unsigned int b = threadIdx.x; b < gridDim.x; b += blockDim.x) t += __ldcg(norm_slots + b);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    if ((threadIdx.x & 31) == 0) red2[threadIdx.x >> 5] = t;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    for (int w = 0; w < kUnscaleThreads / 32; ++w) norm_total += red2[w];
+  } else {
+    if (threadIdx.x != 0) return;
+    if (any_bad) atomicOr(&ws->found, 1);
+    __threadfence();
+    const unsigned int prev = atomicAdd(&ws->arrived, 1u);
+    if (prev != gridDim.x - 1) return;
+    __threadfence();
+  }
+  // Last CTA, thread 0: every flag (and every norm slot) is in; apply the
+  // control loop.
   const int32_t found = atomicOr(&ws->found, 0) != 0;
   float s = *scale;
   int32_t t = *tracker;
@@ -175,6 +262,7 @@ __global__ void __launch_bounds__(kUnscaleThreads)
   *scale = s;
   *tracker = t;
   *found_out = found;
+  if constexpr (NORM) *grad_norm = (float)__dsqrt_rn(norm_total);
   ws->found = 0;
   ws->arrived = 0;
 }
@@ -183,12 +271,19 @@ cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks,
                                         float* scale, int32_t* tracker, int32_t* found,
                                         int64_t* skipped, float growth, float backoff,
                                         int32_t interval, cudaStream_t stream,
-                                        ScalerPolicy policy) {
+                                        ScalerPolicy policy, float* grad_norm,
+                                        double* norm_slots) {
   int64_t grid = (int64_t)sm_count() * kUnscaleCtasPerSm;
   if (grid > n_chunks) grid = n_chunks;
   if (grid < 1) grid = 1;
-  unscale_check_update_kernel<<<(unsigned)grid, kUnscaleThreads, 0, stream>>>(
-      d_chunks, n_chunks, ws, scale, tracker, found, skipped, growth, backoff, interval, policy);
+  if (grad_norm)
+    unscale_check_update_kernel<true><<<(unsigned)grid, kUnscaleThreads, 0, stream>>>(
+        d_chunks, n_chunks, ws, scale, tracker, found, skipped, growth, backoff, interval, policy,
+        grad_norm, norm_slots);
+  else
+    unscale_check_update_kernel<false><<<(unsigned)grid, kUnscaleThreads, 0, stream>>>(
+        d_chunks, n_chunks, ws, scale, tracker, found, skipped, growth, backoff, interval, policy,
+        nullptr, nullptr);
   return cudaGetLastError();
 }
 

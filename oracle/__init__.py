@@ -18,7 +18,8 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SOURCES = ["fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c", "delayed.c"]
+_SOURCES = ["fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c", "delayed.c",
+            "master.c"]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +84,9 @@ def _load():
             "orc_scaler_update_hysteresis": (None, [f32p, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                                     ctypes.POINTER(i64), i32, ctypes.c_float,
                                                     ctypes.c_float, i32, i32, i32, ctypes.c_float]),
+            "orc_sum_squares": (ctypes.c_double, [vp, i64]),
+            "orc_clip_coef": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+            "orc_master_update_sgd": (None, [vp, vp, vp, i64, ctypes.c_float, ctypes.c_float, i32]),
             "orc_e8m0_decode": (ctypes.c_double, [ctypes.c_uint8]),
             "orc_mx_scale_code": (i32, [ctypes.c_double, ctypes.c_int]),
             "orc_quant_mx": (None, [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp]),
@@ -324,3 +328,29 @@ class HysteresisScaler:
                                              ctypes.byref(self.hyst), ctypes.byref(self.skipped),
                                              int(found), growth_factor, backoff_factor, window,
                                              hysteresis, int(consecutive), min_scale)
+
+
+# ---- the consumer step ------------------------------------------------------
+
+def grad_norm(grads: list[np.ndarray]) -> float:
+    """sqrt of the sum of squares over fp32 arrays (compensated, in double)."""
+    tot = 0.0
+    for g in grads:
+        g = np.ascontiguousarray(g, dtype=np.float32)
+        tot += _load().orc_sum_squares(_ptr(g), g.size)
+    return float(np.sqrt(tot))
+
+
+def clip_coef(norm: float, max_norm: float) -> float:
+    return _load().orc_clip_coef(norm, max_norm)
+
+
+def master_update_sgd(w: np.ndarray, g: np.ndarray, lr: float, coef: float, found_inf: int,
+                      want_bf16: bool = True):
+    """In-place SGD step on fp32 master weights w; returns the bf16 copy."""
+    assert w.dtype == np.float32 and w.flags["C_CONTIGUOUS"]
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    wb = np.zeros(w.shape, np.uint16) if want_bf16 else None
+    _load().orc_master_update_sgd(_ptr(w), None if wb is None else _ptr(wb), _ptr(g), w.size, lr,
+                                  coef, int(found_inf))
+    return wb

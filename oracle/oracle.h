@@ -103,6 +103,14 @@ void orc_scaler_update_hysteresis(float* scale, int32_t* tracker, int32_t* hyst,
                                   int32_t window, int32_t hysteresis, int32_t consecutive,
                                   float min_scale);
 
+/* ---- the consumer step: global gradient norm, clipping, FP32 master
+ *      weights ([P3] six-step training step, step 5; [P5] "Range and
+ *      precision"; see master.c) ------------------------------------------ */
+double orc_sum_squares(const float* g, int64_t n);
+float  orc_clip_coef(float norm, float max_norm);
+void   orc_master_update_sgd(float* w, uint16_t* w_bf16, const float* g, int64_t n, float lr,
+                             float coef, int32_t found_inf);
+
 /* Pieces of the block path, exposed so tests can pin each step. */
 float orc_amax(const void* x, int dtype, int64_t n);          /* NaN-propagating */
 float orc_scale_from_amax(float amax, int fmt);               /* max(a,1e-12)/MAX */

@@ -1,0 +1,141 @@
+"""GPU parity for the consumer step: the global gradient norm fused into the
+unscale pass and the FP32 master-weight update that skips on overflow."""
+import numpy as np
+import pytest
+import torch
+
+import datagen as dg
+from datagen import workloads as wl
+from conftest import load_golden
+from gpu_helpers import DEV, assert_same_f32, bits_of, same_bf16, to_dev16
+
+pytestmark = pytest.mark.gpu
+
+NORM_REL_TOL = 35 * 2.0 ** -24     # bound on the sum of squares (see include/gsfp8.h)
+
+
+@pytest.fixture(scope="module")
+def gs():
+    import mixed_precision_numerics_gradscaler_gb300 as gs
+    torch.cuda.set_device(0)
+    return gs
+
+
+def _state(scale=2.0 ** 16):
+    return (torch.tensor([scale], device=DEV), torch.zeros(1, dtype=torch.int32, device=DEV),
+            torch.zeros(1, dtype=torch.int32, device=DEV))
+
+
+def _setup(gs, sizes, step, plant=None):
+    cfg = wl.cfg1_grads()
+    hosts = [dg.fill_host(cfg.spec(t, step), 0, n) for t, n in enumerate(sizes)]
+    if plant:
+        hosts[plant[0]][plant[1]] = 0x7C00
+    grads = [to_dev16(h, torch.float16) for h in hosts]
+    outs = [torch.empty(n, dtype=torch.float32, device=DEV) for n in sizes]
+    return hosts, grads, outs
+
+
+def test_norm_fused_into_unscale(gs, orc):
+    sizes = wl.cfg1_grads().numels
+    hosts, grads, outs = _setup(gs, sizes, 3)
+    outs2 = [torch.empty_like(o) for o in outs]
+    tl = gs.gs_tensor_list_create(grads, outs)
+    tl2 = gs.gs_tensor_list_create(grads, outs2)
+    a, b = _state(), _state()
+    norm = torch.empty(1, dtype=torch.float32, device=DEV)
+    gs.gs_unscale_check_update_norm(tl, *a, norm, None, 2.0, 0.5, 4)
+    gs.gs_unscale_check_update(tl2, *b, None, 2.0, 0.5, 4)
+    torch.cuda.synchronize()
+    for o, o2 in zip(outs, outs2):                 # same outputs and state as the plain step
+        assert (bits_of(o) == bits_of(o2)).all()
+    assert [t.item() for t in a] == [t.item() for t in b]
+    ref_outs, _ = orc.ScalerState(2.0 ** 16).step(hosts, 2.0, 0.5, 4)
+    ref = orc.grad_norm(ref_outs)
+    assert abs(norm.item() ** 2 - ref ** 2) <= NORM_REL_TOL * ref ** 2
+    # bitwise reproducible
+    vals = set()
+    for _ in range(3):
+        a = _state()
+        gs.gs_unscale_check_update_norm(tl, *a, norm, None, 2.0, 0.5, 4)
+        torch.cuda.synchronize()
+        vals.add(bits_of(norm)[0])
+    assert len(vals) == 1
+    tl.close()
+    tl2.close()
+
+
+def test_norm_is_not_finite_on_overflow(gs):
+    sizes = [1000, 5000]
+    _, grads, outs = _setup(gs, sizes, 1, plant=(1, 17))
+    tl = gs.gs_tensor_list_create(grads, outs)
+    st = _state()
+    norm = torch.empty(1, dtype=torch.float32, device=DEV)
+    gs.gs_unscale_check_update_norm(tl, *st, norm, None, 2.0, 0.5, 4)
+    torch.cuda.synchronize()
+    assert st[2].item() == 1 and not np.isfinite(norm.item())
+    tl.close()
+
+
+@pytest.mark.parametrize("max_norm", [0.0, 1e-3, 1e9])
+@pytest.mark.parametrize("with_bf16", [True, False])
+def test_master_update_matches_oracle(gs, orc, max_norm, with_bf16):
+    sizes = [300007, 8192, 77, 16384]
+    hosts, grads, outs = _setup(gs, sizes, 2)
+    tl = gs.gs_tensor_list_create(grads, outs)
+    st = _state()
+    norm = torch.empty(1, dtype=torch.float32, device=DEV)
+    gs.gs_unscale_check_update_norm(tl, *st, norm, None, 2.0, 0.5, 4)
+    rng = np.random.default_rng(5)
+    w_host = [rng.standard_normal(n).astype(np.float32) for n in sizes]
+    w = [torch.from_numpy(x).to(DEV) for x in w_host]
+    wb = [torch.zeros(n, dtype=torch.bfloat16, device=DEV) for n in sizes] if with_bf16 else None
+    pl = gs.gs_param_list_create(w, outs, wb)
+    gs.gs_master_update_sgd(pl, 0.05, max_norm, norm, st[2])
+    torch.cuda.synchronize()
+    coef = orc.clip_coef(norm.item(), max_norm)
+    if max_norm == 1e-3:
+        assert coef < 1.0
+    for i, n in enumerate(sizes):
+        ref_w = w_host[i].copy()
+        ref_b = orc.master_update_sgd(ref_w, outs[i].cpu().numpy(), 0.05, coef, 0)
+        assert_same_f32(w[i].cpu().numpy(), ref_w, f"tensor {i}")
+        if with_bf16:
+            assert same_bf16(bits_of(wb[i]), ref_b).all()
+    pl.close()
+    tl.close()
+
+
+def test_master_update_skips_on_overflow(gs):
+    sizes = [4096, 999]
+    _, grads, outs = _setup(gs, sizes, 4, plant=(0, 5))
+    tl = gs.gs_tensor_list_create(grads, outs)
+    st = _state()
+    norm = torch.empty(1, dtype=torch.float32, device=DEV)
+    gs.gs_unscale_check_update_norm(tl, *st, norm, None, 2.0, 0.5, 4)
+    w = [torch.full((n,), 3.0, device=DEV) for n in sizes]
+    wb = [torch.zeros(n, dtype=torch.bfloat16, device=DEV) for n in sizes]
+    pl = gs.gs_param_list_create(w, outs, wb)
+    gs.gs_master_update_sgd(pl, 0.1, 1.0, norm, st[2])
+    torch.cuda.synchronize()
+    assert st[2].item() == 1
+    assert all(bool((x == 3.0).all()) for x in w) and all(bool((x == 0).all()) for x in wb)
+    pl.close()
+    tl.close()
+
+
+def test_printed_master_weight_demo_on_the_device(gs):
+    """precision.py's fp32 master weight: 1.0 plus 1e-3, 1000 times, prints
+    2.0000; its bf16 copy follows it."""
+    g = load_golden("p5_precision_py_output.json")
+    w = torch.ones(8, device=DEV)
+    wb = torch.zeros(8, dtype=torch.bfloat16, device=DEV)
+    grad = torch.full((8,), -g["update"], device=DEV)
+    found = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pl = gs.gs_param_list_create([w], [grad], [wb])
+    for _ in range(g["n_updates"]):
+        gs.gs_master_update_sgd(pl, 1.0, 0.0, None, found)
+    torch.cuda.synchronize()
+    assert f"{w[0].item():.4f}" == g["fp32_weight_after"]
+    assert f"{wb[0].float().item():.4f}" == "2.0000"
+    pl.close()

@@ -251,3 +251,29 @@ def test_cfg2_llama3_8b_full_size_sampled(gs, orc):
     tl.close()
     del grads, outs
     torch.cuda.empty_cache()
+
+
+def test_reciprocal_of_the_scale_for_many_scales(gs):
+    """Unscaling a 1.0 exposes fp32(1/S) itself: it must equal the oracle's
+    (float)(1.0 / (double)S) for every power of two and for random scales,
+    subnormal ones included."""
+    rng = np.random.default_rng(9)
+    pows = [2.0 ** k for k in range(-149, 128)]
+    rand = rng.integers(1, 0x7F800000, size=2500, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    scales = np.array(pows + rand.tolist(), np.float32)
+    g = to_dev16(np.array([0x3C00], np.uint16), torch.float16)       # 1.0
+    o = torch.empty(1, dtype=torch.float32, device=DEV)
+    tl = gs.gs_tensor_list_create([g], [o])
+    sc = torch.empty(1, dtype=torch.float32, device=DEV)
+    tr = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fi = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = torch.empty(scales.size, dtype=torch.float32, device=DEV)
+    for i, s in enumerate(scales):
+        sc.fill_(float(s))
+        gs.gs_unscale_check_update(tl, sc, tr, fi, None, 1.0, 1.0, 1)
+        got[i:i + 1].copy_(o)
+    with np.errstate(over="ignore"):                 # 1/S overflows for S < 2^-128
+        want = (1.0 / scales.astype(np.float64)).astype(np.float32)
+    torch.cuda.synchronize()
+    assert_same_f32(got.cpu().numpy(), want, "fp32(1/S)")
+    tl.close()

@@ -16,7 +16,7 @@ from conftest import ROOT
 
 ORACLE = os.path.join(ROOT, "oracle")
 PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_scaler.py", "tests/test_oracle_quant.py",
-        "tests/test_oracle_mx.py", "tests/test_oracle_delayed.py"]
+        "tests/test_oracle_mx.py", "tests/test_oracle_delayed.py", "tests/test_oracle_master.py"]
 
 MUTANTS = {
     "ties round up instead of to even": (
@@ -58,6 +58,13 @@ MUTANTS = {
         "delayed.c", "    if (!consecutive) *hyst = hysteresis;\n", ""),
     "min loss scale ignored": (
         "delayed.c", "*scale = s < min_scale ? min_scale : s;", "*scale = s;"),
+    "skipped step applied": (
+        "master.c", "if (found_inf) return;", ""),
+    "clip coefficient inverted": (
+        "master.c", "return max_norm / norm;", "return norm / max_norm;"),
+    "update by the fused form": (
+        "master.c", "float t1 = coef * g[i];\n    float t2 = lr * t1;\n    w[i] = w[i] - t2;",
+        "w[i] = fmaf(-lr, coef * g[i], w[i]);"),
     "dequant scale index transposed": (
         "fp8_quant.c", "float s = scales[(r / br) * nbc + c / bc];", "float s = scales[(c / bc) * (R / br) + r / br];"),
 }
@@ -66,7 +73,8 @@ MUTANTS = {
 def _build_variant(tmp, name, patch):
     d = os.path.join(tmp, name.replace(" ", "_").replace("(", "").replace(")", "").replace(",", ""))
     os.makedirs(d)
-    for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c", "delayed.c"]:
+    for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c", "delayed.c",
+              "master.c"]:
         shutil.copy(os.path.join(ORACLE, f), d)
     if patch is not None:
         fname, old, new = patch
@@ -78,7 +86,7 @@ def _build_variant(tmp, name, patch):
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
                     "-shared", "-o", lib, *[os.path.join(d, f) for f in
                                             ["fp_formats.c", "gradscaler.c", "fp8_quant.c",
-                                             "mx_quant.c", "delayed.c"]], "-lm"],
+                                             "mx_quant.c", "delayed.c", "master.c"]], "-lm"],
                    check=True)
     return lib
 
@@ -91,6 +99,7 @@ PINS_FOR = {
     "fp8_quant.c": ["tests/test_oracle_quant.py", "tests/test_oracle_delayed.py"],
     "mx_quant.c": ["tests/test_oracle_mx.py"],
     "delayed.c": ["tests/test_oracle_delayed.py"],
+    "master.c": ["tests/test_oracle_master.py"],
 }
 
 
