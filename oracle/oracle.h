@@ -111,6 +111,14 @@ float  orc_clip_coef(float norm, float max_norm);
 void   orc_master_update_sgd(float* w, uint16_t* w_bf16, const float* g, int64_t n, float lr,
                              float coef, int32_t found_inf);
 
+/* ---- the GEMM that consumes the tiles, FP32 promotion every 128 of K
+ *      ([P1] "FP8 needs a finer-grained fix"; [P5] "FP8 training"; see
+ *      gemm.c) ------------------------------------------------------------ */
+double orc_gemm_fp8_block_elem(const uint8_t* qa, const float* sa, const uint8_t* qb,
+                               const float* sb, int64_t K, int64_t m, int64_t n, int fmt);
+void orc_gemm_fp8_block(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                        int64_t M, int64_t N, int64_t K, int fmt, double* d);
+
 /* Pieces of the block path, exposed so tests can pin each step. */
 float orc_amax(const void* x, int dtype, int64_t n);          /* NaN-propagating */
 float orc_scale_from_amax(float amax, int fmt);               /* max(a,1e-12)/MAX */

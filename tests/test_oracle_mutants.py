@@ -16,7 +16,8 @@ from conftest import ROOT
 
 ORACLE = os.path.join(ROOT, "oracle")
 PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_scaler.py", "tests/test_oracle_quant.py",
-        "tests/test_oracle_mx.py", "tests/test_oracle_delayed.py", "tests/test_oracle_master.py"]
+        "tests/test_oracle_mx.py", "tests/test_oracle_delayed.py", "tests/test_oracle_master.py",
+        "tests/test_oracle_gemm.py"]
 
 MUTANTS = {
     "ties round up instead of to even": (
@@ -65,6 +66,10 @@ MUTANTS = {
     "update by the fused form": (
         "master.c", "float t1 = coef * g[i];\n    float t2 = lr * t1;\n    w[i] = w[i] - t2;",
         "w[i] = fmaf(-lr, coef * g[i], w[i]);"),
+    "GEMM weight scale indexed by row instead of block": (
+        "gemm.c", "(double)sb[(n / 128) * nkb + kb]", "(double)sb[n * nkb + kb]"),
+    "GEMM promotion with one block's scale for all": (
+        "gemm.c", "(double)sa[m * nkb + kb]", "(double)sa[m * nkb]"),
     "dequant scale index transposed": (
         "fp8_quant.c", "float s = scales[(r / br) * nbc + c / bc];", "float s = scales[(c / bc) * (R / br) + r / br];"),
 }
@@ -74,7 +79,7 @@ def _build_variant(tmp, name, patch):
     d = os.path.join(tmp, name.replace(" ", "_").replace("(", "").replace(")", "").replace(",", ""))
     os.makedirs(d)
     for f in ["oracle.h", "fp_formats.c", "gradscaler.c", "fp8_quant.c", "mx_quant.c", "delayed.c",
-              "master.c"]:
+              "master.c", "gemm.c"]:
         shutil.copy(os.path.join(ORACLE, f), d)
     if patch is not None:
         fname, old, new = patch
@@ -86,7 +91,8 @@ def _build_variant(tmp, name, patch):
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
                     "-shared", "-o", lib, *[os.path.join(d, f) for f in
                                             ["fp_formats.c", "gradscaler.c", "fp8_quant.c",
-                                             "mx_quant.c", "delayed.c", "master.c"]], "-lm"],
+                                             "mx_quant.c", "delayed.c", "master.c", "gemm.c"]],
+                   "-lm"],
                    check=True)
     return lib
 
@@ -100,6 +106,7 @@ PINS_FOR = {
     "mx_quant.c": ["tests/test_oracle_mx.py"],
     "delayed.c": ["tests/test_oracle_delayed.py"],
     "master.c": ["tests/test_oracle_master.py"],
+    "gemm.c": ["tests/test_oracle_gemm.py"],
 }
 
 
