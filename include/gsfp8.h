@@ -308,6 +308,41 @@ int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C
                    int out_dtype, void* y, void* stream);
 
 /* ------------------------------------------------------------------------
+ * The consumer of the block-scaled tiles: an FP8 GEMM whose partial sums are
+ * promoted to FP32 every 128 elements of K ([P1] "FP8 needs a
+ * finer-grained fix than a single scale factor": the tensor cores'
+ * accumulator keeps too few bits, so partial sums move to FP32 registers at
+ * intervals; [P5] "FP8 training": promotion every 128 elements, 1x128
+ * scales for activations, 128x128 for weights).
+ * --------------------------------------------------------------------- */
+
+/* D = A B^T with A = decode(qa) scaled per 1x128 block and B = decode(qb)
+ * scaled per 128x128 block:
+ *   D[m][n] = sum over kb of sa[m][kb] * sb[n / 128][kb] * P[m][n][kb],
+ *   P[m][n][kb] = sum over k in [128 kb, 128 kb + 128) of
+ *                 decode(qa[m][k]) * decode(qb[n][k]).
+ * P is formed by the tensor cores (fp32 accumulator, order inside a block
+ * not specified); the promotion is one fp32 fused multiply-add per block,
+ * acc = fma(P, fp32(sa * sb), acc), in increasing kb.
+ *   qa: row-major [M, K] codes, sa: row-major [M, K / 128] fp32 (as
+ *       fp8_quant_block writes for block (1, 128));
+ *   qb: row-major [N, K] codes (the weight stored [out, in]), sb:
+ *       row-major [ceil(N / 128), K / 128] fp32 (block (128, 128));
+ *   fmt: GS_E4M3 or GS_E5M2, the format of both operands;
+ *   d: row-major [M, N], out_dtype GS_F32 or GS_BF16 (rounded to nearest
+ *      even from the fp32 sum).
+ * K % 128 == 0 and M <= 65535 * 128 (else GS_ERR_SHAPE); M and N need not
+ * be multiples of 128; K == 0 writes zeros.  qa and qb must be 16-byte
+ * aligned (they are read by TMA; else GS_ERR_ARG).  Accuracy against the
+ * exact sum: |error| <= (2^-24 * (nkb + 3) + e_blk) * sum over kb of
+ * |sa sb| sum over k |a b|, e_blk being the tensor cores' relative
+ * accumulation error within one block.  A wait that runs out records
+ * GS_ERR_TIMEOUT (gs_device_status) and leaves d unspecified. */
+int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                          int64_t M, int64_t N, int64_t K, int fmt, int out_dtype, void* d,
+                          void* stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  * --------------------------------------------------------------------- */
 

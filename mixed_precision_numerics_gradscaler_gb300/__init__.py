@@ -38,10 +38,10 @@ def lib_path() -> str:
 
 
 def _load_lib() -> ctypes.CDLL:
-    if not os.path.exists(_build.LIB):
+    if not _build.up_to_date():
         if os.environ.get("GSFP8_BUILD_ON_IMPORT", "1") == "1":
             _build.build()
-        else:
+        elif not os.path.exists(_build.LIB):
             raise ImportError(f"libgsfp8.so not built ({_build.LIB}); run __graft_entry__.build()")
     lib = ctypes.CDLL(_build.LIB)
     i32, i64, vp, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
@@ -72,6 +72,7 @@ def _load_lib() -> ctypes.CDLL:
         "fp8_dequant_mx": (ci, [vp, vp, i64, i64, ci, ci, vp, vp]),
         "gs_unscale_check_update_noalloc": (ci, [vp, vp, vp, i32, vp, vp, vp, vp, f32, f32, i32, vp]),
         "gs_noalloc_limits": (ci, [ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64)]),
+        "fp8_gemm_block_scaled": (ci, [vp, vp, vp, vp, i64, i64, i64, ci, ci, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -348,6 +349,21 @@ def fp8_dequant_mx(q: torch.Tensor, scales: torch.Tensor, fmt, y: torch.Tensor, 
     R, C = q.shape
     _check(_lib.fp8_dequant_mx(_ptr(q), _ptr(scales), R, C, _FMTS[fmt], _DTYPES[y.dtype], _ptr(y),
                                _stream(stream)), "fp8_dequant_mx")
+
+
+def fp8_gemm_block_scaled(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
+                          fmt, d: torch.Tensor, stream=None) -> None:
+    """d[M, N] = block-scaled qa[M, K] @ qb[N, K]^T, promoted to fp32 every 128 of K."""
+    for t, name in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb"), (d, "d")):
+        _contig(t, name)
+    M, K = qa.shape
+    N = qb.shape[0]
+    if qb.shape[1] != K or tuple(d.shape) != (M, N):
+        raise ValueError(f"fp8_gemm_block_scaled: shapes qa {tuple(qa.shape)}, "
+                         f"qb {tuple(qb.shape)}, d {tuple(d.shape)}")
+    _check(_lib.fp8_gemm_block_scaled(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _FMTS[fmt],
+                                      _DTYPES[d.dtype], _ptr(d), _stream(stream)),
+           "fp8_gemm_block_scaled")
 
 
 def gs_device_status(stream=None) -> int:

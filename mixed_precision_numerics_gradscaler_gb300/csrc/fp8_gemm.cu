@@ -1,0 +1,387 @@
+// fp8_gemm.cu -- the consumer of the block-scaled FP8 tiles: a GEMM on the
+// 5th-generation tensor cores whose FP8 partial sums are promoted to FP32
+// with their scales every 128 elements of K ("Loss scaling, FP8, and the
+// failure that never crashes", section "FP8 needs a finer-grained fix than a
+// single scale factor": periodic promotion to FP32 accumulation; "Mixed
+// precision and FP8 training", section "FP8 training": promotion every 128
+// elements, activations with 1x128 scales, weights with 128x128 scales).
+//
+//   D[m][n] = sum_kb sa[m][kb] * sb[n/128][kb] * sum_{k in kb} A[m][k] * B[n][k]
+//
+// A = [M, K] and B = [N, K] FP8 codes (both K-major, as fp8_quant_block
+// writes them), D = [M, N] fp32 or bf16.  One CTA per 128x128 tile of D,
+// warp-specialised:
+//   warp 0 (one lane)  TMA loads of 128x128-byte A and B tiles (128-byte
+//                      swizzle, no multicast) into a 4-stage ring;
+//   warp 1             allocates 256 TMEM columns; one lane issues, per
+//                      128-wide K-block, four tcgen05.mma.kind::f8f6f4
+//                      (M 128, N 128, K 32) into one of two TMEM
+//                      accumulators, then commits to the stage's "empty"
+//                      barrier and the accumulator's "full" barrier;
+//   warps 2-5          read each block's 128x128 fp32 partial from TMEM
+//                      (tcgen05.ld, one row per thread), multiply by
+//                      sa * sb and add into fp32 registers (the promotion),
+//                      release the accumulator, and finally store D.
+// Every mbarrier wait is bounded by %globaltimer; a role that gives up sets
+// a shared abort flag and GS_ERR_TIMEOUT, the others leave their loops, the
+// MMA lane and the TMA lane wait (bounded) for their own work in flight, and
+// the TMEM columns are freed on every path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+constexpr int kGB = 128;                 // tile M = N = K-block
+constexpr int kGStages = 4;
+constexpr int kGThreads = 192;
+constexpr int kGTile = kGB * kGB;        // bytes of one FP8 operand tile
+constexpr int kGTmemCols = 256;          // two 128-column fp32 accumulators
+constexpr int kGSmemBytes = 2 * kGStages * kGTile + 1024 + 256;
+constexpr uint64_t kGWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t g_smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t g_now() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool g_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(g_smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; gives up on timeout (setting the abort flag and the status)
+// or when another role has already aborted.
+__device__ __forceinline__ bool g_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                       int32_t* status) {
+  if (g_try_wait(bar, parity)) return true;
+  const uint64_t t0 = g_now();
+  while (!g_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (g_now() - t0 > kGWaitNs) {
+      *abort_flag = 1;
+      atomicExch(status, (int32_t)GS_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// Bounded wait that ignores the abort flag (draining own work in flight).
+__device__ __forceinline__ void g_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = g_now();
+  while (!g_try_wait(bar, parity))
+    if (g_now() - t0 > kGWaitNs) return;
+}
+__device__ __forceinline__ void g_bar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(g_smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void g_bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(g_smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void g_tma_load(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                           int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(g_smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(g_smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte
+// swizzled layout that TMA writes: rows of 128 bytes, 8-row groups 1024
+// bytes apart (stride byte offset), descriptor version 1, swizzle mode
+// 128B.  The leading byte offset is unused for swizzled K-major tiles.
+__device__ __forceinline__ uint64_t umma_desc_k_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f8f6f4: fp32 accumulator, A and B of the
+// given FP8 format (0 E4M3, 1 E5M2), both K-major, N = 128, M = 128.
+__host__ __device__ constexpr uint32_t umma_idesc_f8(uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kGB >> 3) << 17) |
+         ((uint32_t)(kGB >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          g_smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns of TMEM -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+template <int FMT, int OUT>
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_fp8_block_scaled(const __grid_constant__ CUtensorMap map_a,
+                          const __grid_constant__ CUtensorMap map_b, const float* __restrict__ sa,
+                          const float* __restrict__ sb, int64_t M, int64_t N, int64_t K,
+                          int vec_store, void* __restrict__ d, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment of the swizzled tiles
+  const uint32_t pad = (1024u - (g_smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* tiles = smem_raw + pad;
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + 2 * kGStages * kGTile);
+  uint64_t* empty = full + kGStages;
+  uint64_t* tfull = empty + kGStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t n0 = (int64_t)blockIdx.x * kGB, m0 = (int64_t)blockIdx.y * kGB;
+  const int nkb = (int)((K + kGB - 1) / kGB);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      g_bar_init(&full[s], 1);
+      g_bar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      g_bar_init(&tfull[b], 1);
+      g_bar_init(&tempty[b], 128);
+    }
+    g_bar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     g_smem_u32(tmem_slot)),
+                 "r"(kGTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kGStages;
+        const uint32_t ph = (uint32_t)((kb / kGStages) & 1);
+        if (!g_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                         g_smem_u32(&full[s])),
+                     "r"(2 * kGTile)
+                     : "memory");
+        g_tma_load(&map_a, &full[s], tiles + s * kGTile, kb * kGB, (int32_t)m0);
+        g_tma_load(&map_b, &full[s], tiles + (kGStages + s) * kGTile, kb * kGB, (int32_t)n0);
+        ++issued;
+      }
+      // Let the last load of every stage land before the CTA can exit (they
+      // have landed already unless another role gave up).
+      for (int j = (issued > kGStages ? issued - kGStages : 0); j < issued; ++j)
+        g_drain(&full[j % kGStages], (uint32_t)((j / kGStages) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      constexpr uint32_t idesc = umma_idesc_f8((uint32_t)FMT);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kGStages, b = kb & 1;
+        const uint32_t ph = (uint32_t)((kb / kGStages) & 1), tph = (uint32_t)((kb >> 1) & 1);
+        if (!g_wait(&full[s], ph, abort_flag, status)) break;
+        if (!g_wait(&tempty[b], tph ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t a0 = g_smem_u32(tiles + s * kGTile);
+        const uint32_t b0 = g_smem_u32(tiles + (kGStages + s) * kGTile);
+#pragma unroll
+        for (int kk = 0; kk < kGB / 32; ++kk)
+          umma_f8(tmem + (uint32_t)(b * kGB), umma_desc_k_sw128(a0 + 32 * kk),
+                  umma_desc_k_sw128(b0 + 32 * kk), idesc, kk > 0 ? 1u : 0u);
+        umma_commit(&empty[s]);
+        umma_commit(&tfull[b]);
+      }
+      umma_commit(drain);  // completes when every MMA issued above has
+      g_drain(drain, 0);
+    }
+  } else {  // promotion and store: warps 2..5, one TMEM lane (row) per thread
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const bool row_ok = m0 + row < M;  // rows past M were loaded as zeros
+    const float* sa_row = sa + (row_ok ? (m0 + row) * nkb : 0);
+    const float* sb_row = sb + (n0 / kGB) * nkb;
+    float acc[kGB];
+#pragma unroll
+    for (int j = 0; j < kGB; ++j) acc[j] = 0.0f;
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int b = kb & 1;
+      const uint32_t tph = (uint32_t)((kb >> 1) & 1);
+      // the warp leaves together: tcgen05.ld below needs all 32 lanes
+      const bool got = g_wait(&tfull[b], tph, abort_flag, status);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float sc = row_ok ? __fmul_rn(sa_row[kb], sb_row[kb]) : 0.0f;
+#pragma unroll
+      for (int c = 0; c < kGB / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kGB + 32 * c), v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[32 * c + j] = __fmaf_rn(v[j], sc, acc[32 * c + j]);
+      }
+      tc_fence_before();
+      g_bar_arrive(&tempty[b]);
+    }
+    if (ok && !*abort_flag && row_ok) {
+      const int64_t off = (m0 + row) * N + n0;
+      if (vec_store && n0 + kGB <= N) {
+        if constexpr (OUT == GS_F32) {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(d) + off);
+#pragma unroll
+          for (int j = 0; j < kGB / 4; ++j)
+            dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(d) + off);
+#pragma unroll
+          for (int j = 0; j < kGB / 8; ++j)
+            dst[j] = make_uint4(cvt_f32x2_bf16x2(acc[8 * j + 1], acc[8 * j]),
+                                cvt_f32x2_bf16x2(acc[8 * j + 3], acc[8 * j + 2]),
+                                cvt_f32x2_bf16x2(acc[8 * j + 5], acc[8 * j + 4]),
+                                cvt_f32x2_bf16x2(acc[8 * j + 7], acc[8 * j + 6]));
+        }
+      } else {  // ragged N or unaligned D: one element at a time
+#pragma unroll
+        for (int j = 0; j < kGB; ++j) {
+          if (n0 + j < N) {
+            if constexpr (OUT == GS_F32)
+              reinterpret_cast<float*>(d)[off + j] = acc[j];
+            else
+              reinterpret_cast<uint16_t*>(d)[off + j] =
+                  (uint16_t)(cvt_f32x2_bf16x2(0.0f, acc[j]) & 0xFFFFu);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kGTmemCols)
+                 : "memory");
+  }
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+static CUresult encode_k_major(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K) {
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {kGB, kGB};
+  const cuuint32_t estr[2] = {1, 1};
+  return gemm_encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int FMT, int OUT>
+static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const float* sa,
+                          const float* sb, int64_t M, int64_t N, int64_t K, int vec_store,
+                          void* d, int32_t* status, cudaStream_t st) {
+  auto k = gemm_fp8_block_scaled<FMT, OUT>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const dim3 grid((unsigned)((N + kGB - 1) / kGB), (unsigned)((M + kGB - 1) / kGB));
+  k<<<grid, kGThreads, kGSmemBytes, st>>>(ma, mb, sa, sb, M, N, K, vec_store, d, status);
+  return cudaGetLastError();
+}
+
+// The caller has checked: qa and qb 16-byte aligned, K a multiple of 16
+// (the tensor maps' row stride), M and N below 2^31 / 128 tiles.  Returns
+// cudaErrorNotSupported when the tensor-map entry point is missing.
+cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
+                                         const float* sb, int64_t M, int64_t N, int64_t K, int fmt,
+                                         int out_dtype, void* d, int32_t* status,
+                                         cudaStream_t st) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const size_t esz = out_dtype == GS_F32 ? 4 : 2;
+  if (K == 0) return cudaMemsetAsync(d, 0, (size_t)M * (size_t)N * esz, st);  // empty sums
+  if (!gemm_encode_fn()) return cudaErrorNotSupported;
+  CUtensorMap ma, mb;
+  if (encode_k_major(&ma, qa, M, K) != CUDA_SUCCESS || encode_k_major(&mb, qb, N, K) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int vec = (N % 8 == 0) && ((uintptr_t)d % 16 == 0);
+  if (fmt == GS_E4M3)
+    return out_dtype == GS_F32
+               ? gemm_t<GS_E4M3, GS_F32>(ma, mb, sa, sb, M, N, K, vec, d, status, st)
+               : gemm_t<GS_E4M3, GS_BF16>(ma, mb, sa, sb, M, N, K, vec, d, status, st);
+  return out_dtype == GS_F32 ? gemm_t<GS_E5M2, GS_F32>(ma, mb, sa, sb, M, N, K, vec, d, status, st)
+                             : gemm_t<GS_E5M2, GS_BF16>(ma, mb, sa, sb, M, N, K, vec, d, status, st);
+}
+
+}  // namespace gs

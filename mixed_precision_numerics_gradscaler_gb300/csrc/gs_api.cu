@@ -483,6 +483,38 @@ int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
 
+int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                          int64_t M, int64_t N, int64_t K, int fmt, int out_dtype, void* d,
+                          void* stream) {
+  if (!valid_fmt(fmt) || !(out_dtype == GS_F32 || out_dtype == GS_BF16)) return GS_ERR_DTYPE;
+  if (M < 0 || N < 0 || K < 0 || K % 128 != 0 || M > 65535LL * 128 || K >= (1LL << 31) ||
+      N >= (1LL << 31) || !mul_ok(M, N) || !mul_ok(M * N, 4) || !mul_ok(M, K) || !mul_ok(N, K))
+    return GS_ERR_SHAPE;
+  if (M == 0 || N == 0) return GS_OK;
+  if (!d || (K > 0 && (!qa || !sa || !qb || !sb))) return GS_ERR_NULL;
+  const size_t dsz = out_dtype == GS_F32 ? 4 : 2, nd = (size_t)(M * N) * dsz;
+  if (!aligned(d, dsz)) return GS_ERR_ARG;
+  if (!device_reachable(d)) return GS_ERR_ARG;
+  if (K > 0) {
+    const int64_t nkb = K / 128;
+    const size_t na = (size_t)(M * K), nb = (size_t)(N * K);
+    const size_t nsa = (size_t)(M * nkb) * 4, nsb = (size_t)(((N + 127) / 128) * nkb) * 4;
+    if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 4) || !aligned(sb, 4))
+      return GS_ERR_ARG;
+    if (!device_reachable(qa) || !device_reachable(sa) || !device_reachable(qb) ||
+        !device_reachable(sb))
+      return GS_ERR_ARG;
+    if (overlaps(d, nd, qa, na) || overlaps(d, nd, qb, nb) || overlaps(d, nd, sa, nsa) ||
+        overlaps(d, nd, sb, nsb))
+      return GS_ERR_ARG;
+  }
+  int32_t* status = device_status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+  cudaError_t e = launch_gemm_fp8_block_scaled(qa, sa, qb, sb, M, N, K, fmt, out_dtype, d, status,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
 int gs_device_status(int32_t* h_status, void* stream) {
   if (!h_status) return GS_ERR_NULL;
   int32_t* p = device_status_ptr();

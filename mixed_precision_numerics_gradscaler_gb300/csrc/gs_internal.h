@@ -85,6 +85,10 @@ cudaError_t launch_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R
 cudaError_t launch_quant_tensor_delayed(const void* x, int dtype, int64_t n, int fmt, uint8_t* q,
                                         float* history, int hist_len, int32_t* pos,
                                         float* scale_used, uint32_t* partials, cudaStream_t stream);
+cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
+                                         const float* sb, int64_t M, int64_t N, int64_t K, int fmt,
+                                         int out_dtype, void* d, int32_t* status,
+                                         cudaStream_t stream);
 cudaError_t launch_set_state(float* scale, int32_t* tracker, float h_scale, int32_t h_tracker,
                              cudaStream_t stream);
 

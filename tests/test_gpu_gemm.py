@@ -1,0 +1,207 @@
+"""GPU parity of the block-scaled FP8 GEMM with FP32 promotion against the
+oracle ("Mixed precision and FP8 training", section "FP8 training";
+"Loss scaling, FP8, and the failure that never crashes", section "FP8
+needs a finer-grained fix than a single scale factor").
+
+Two kinds of case:
+  * exact: FP8 values in {-2, -1, 0, 1, 2} and power-of-two scales, so every
+    partial sum, product and promotion step is exact in fp32 whatever the
+    order of the tensor cores' additions -- the result must equal the
+    oracle bit for bit.  Any layout mistake (swizzle, K advance, operand
+    transposed, wrong scale index, wrong TMEM lane) changes some value.
+  * general: every finite FP8 code and real-valued scales; the error against
+    the exact sum must stay within
+        tol = (2^-24 * (nkb + 3) + E_BLK) * sum_kb |sa sb| sum_k |a b|
+    (fp32 promotion: one rounding of sa*sb and one per fused multiply-add in
+    a chain of nkb; E_BLK bounds the tensor cores' relative error inside one
+    128-element block, 2^-24 * 128 = the textbook bound of 128 fp32
+    additions).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import DEV, bits_of
+
+pytestmark = pytest.mark.gpu
+
+E4M3, E5M2, F32, BF16 = 0, 1, 2, 1
+E_BLK = 2.0 ** -24 * 128
+
+
+@pytest.fixture(scope="module")
+def gs():
+    import mixed_precision_numerics_gradscaler_gb300 as m
+    return m
+
+
+def _finite_codes(orc, fmt):
+    vals = orc.fp8_decode_array(np.arange(256, dtype=np.uint8), fmt)
+    return np.flatnonzero(np.isfinite(vals)).astype(np.uint8)
+
+
+def _codes_of(orc, fmt, values):
+    """Code of each value (exactly representable) via the oracle's decoder."""
+    table = orc.fp8_decode_array(np.arange(256, dtype=np.uint8), fmt)
+    out = {}
+    for v in values:
+        hits = np.flatnonzero(table == v)
+        out[v] = int(hits[0] if v != 0 else 0)
+    return out
+
+
+def _exact_inputs(orc, fmt, M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    cmap = _codes_of(orc, fmt, [-2.0, -1.0, 0.0, 1.0, 2.0])
+    lut = np.array([cmap[v] for v in (-2.0, -1.0, 0.0, 1.0, 2.0)], np.uint8)
+    qa = lut[rng.integers(0, 5, (M, K))]
+    qb = lut[rng.integers(0, 5, (N, K))]
+    nkb = K // 128
+    sa = np.exp2(rng.integers(-2, 3, (M, nkb))).astype(np.float32)
+    sb = np.exp2(rng.integers(-2, 3, ((N + 127) // 128, nkb))).astype(np.float32)
+    return qa, sa, qb, sb
+
+
+def _general_inputs(orc, fmt, M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    codes = _finite_codes(orc, fmt)
+    qa = codes[rng.integers(0, len(codes), (M, K))]
+    qb = codes[rng.integers(0, len(codes), (N, K))]
+    nkb = K // 128
+    sa = rng.lognormal(-4.0, 2.0, (M, nkb)).astype(np.float32)
+    sb = rng.lognormal(-6.0, 2.0, ((N + 127) // 128, nkb)).astype(np.float32)
+    return qa, sa, qb, sb
+
+
+def _run(gs, qa, sa, qb, sb, fmt, out_dtype):
+    M, N = qa.shape[0], qb.shape[0]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    d = torch.full((M, N), float("nan"), dtype=torch.float32 if out_dtype == F32 else torch.bfloat16,
+                   device=DEV)
+    gs.fp8_gemm_block_scaled(t(qa), t(sa), t(qb), t(sb), fmt, d)
+    torch.cuda.synchronize()
+    assert gs.gs_device_status() == 0
+    return d
+
+
+def _assert_exact(orc, got, want_f64, out_dtype, what):
+    want32 = want_f64.astype(np.float32)
+    assert (want32.astype(np.float64) == want_f64).all(), "exact case is not exact in fp32"
+    if out_dtype == F32:
+        g = got.cpu().numpy()
+        bad = g.view(np.uint32) != want32.view(np.uint32)
+    else:
+        g = bits_of(got)
+        bad = g != orc.encode_array(want_f64, BF16)
+    if bad.any():
+        i = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} differ, first at {i.tolist()}")
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (300, 200, 1280),
+                                   (1, 128, 128), (129, 1, 256), (130, 260, 640)])
+def test_gemm_exact_values_bit_exact(gs, orc, fmt, M, N, K):
+    qa, sa, qb, sb = _exact_inputs(orc, fmt, M, N, K, seed=M * 7 + N * 3 + K + fmt)
+    want = orc.gemm_fp8_block(qa, sa, qb, sb, fmt)
+    got = _run(gs, qa, sa, qb, sb, fmt, F32)
+    _assert_exact(orc, got, want, F32, f"fmt {fmt} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_gemm_exact_values_bf16_output(gs, orc, fmt):
+    qa, sa, qb, sb = _exact_inputs(orc, fmt, 384, 512, 768, seed=11 + fmt)
+    want = orc.gemm_fp8_block(qa, sa, qb, sb, fmt)
+    got = _run(gs, qa, sa, qb, sb, fmt, BF16)
+    _assert_exact(orc, got, want, BF16, f"bf16 fmt {fmt}")
+
+
+def _tolerance(orc, qa, sa, qb, sb, fmt):
+    absd = orc.gemm_fp8_block(qa & 0x7F, sa, qb & 0x7F, sb, fmt)
+    nkb = qa.shape[1] // 128
+    return (2.0 ** -24 * (nkb + 3) + E_BLK) * absd
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 1024), (200, 136, 2048)])
+def test_gemm_general_codes_within_bound(gs, orc, fmt, M, N, K):
+    qa, sa, qb, sb = _general_inputs(orc, fmt, M, N, K, seed=1000 + M + N + K + fmt)
+    want = orc.gemm_fp8_block(qa, sa, qb, sb, fmt)
+    tol = _tolerance(orc, qa, sa, qb, sb, fmt)
+    got = _run(gs, qa, sa, qb, sb, fmt, F32).cpu().numpy().astype(np.float64)
+    err = np.abs(got - want)
+    assert np.isfinite(got).all()
+    assert (err <= tol).all(), f"max err/tol {np.max(err / np.maximum(tol, 1e-300)):.3f}"
+
+
+def test_gemm_k_zero_writes_zeros(gs):
+    qa = torch.empty((5, 0), dtype=torch.uint8, device=DEV)
+    qb = torch.empty((7, 0), dtype=torch.uint8, device=DEV)
+    sa = torch.empty((5, 0), dtype=torch.float32, device=DEV)
+    sb = torch.empty((1, 0), dtype=torch.float32, device=DEV)
+    d = torch.full((5, 7), 3.0, device=DEV)
+    gs.fp8_gemm_block_scaled(qa, sa, qb, sb, E4M3, d)
+    torch.cuda.synchronize()
+    assert (d == 0).all()
+
+
+def test_gemm_rejects_bad_arguments(gs):
+    qa = torch.zeros((128, 256), dtype=torch.uint8, device=DEV)
+    qb = torch.zeros((128, 256), dtype=torch.uint8, device=DEV)
+    sa = torch.ones((128, 2), device=DEV)
+    sb = torch.ones((1, 2), device=DEV)
+    d = torch.zeros((128, 128), device=DEV)
+    # K not a multiple of 128
+    with pytest.raises(gs.GsError):
+        gs.fp8_gemm_block_scaled(qa[:, :200].contiguous(), sa, qb[:, :200].contiguous(), sb, E4M3, d)
+    # operand not 16-byte aligned (TMA)
+    buf = torch.zeros(128 * 256 + 16, dtype=torch.uint8, device=DEV)
+    qa_off = buf[1:1 + 128 * 256].view(128, 256)
+    with pytest.raises(gs.GsError):
+        gs.fp8_gemm_block_scaled(qa_off, sa, qb, sb, E4M3, d)
+    # output overlapping an input
+    d_buf = torch.zeros((128, 128), device=DEV)
+    qa_alias = d_buf.view(torch.uint8).view(-1)[:128 * 256].view(128, 256)
+    with pytest.raises(gs.GsError):
+        gs.fp8_gemm_block_scaled(qa_alias, sa, qb, sb, E4M3, d_buf)
+    # output dtype other than fp32 / bf16
+    with pytest.raises(gs.GsError):
+        gs.fp8_gemm_block_scaled(qa, sa, qb, sb, E4M3, d.to(torch.float16))
+    torch.cuda.synchronize()
+    assert gs.gs_device_status() == 0
+
+
+def test_gemm_full_size_sampled(gs, orc):
+    """The benchmarked shape and launch (activations 16384 x 8192, weight
+    28672 x 8192, E4M3, bf16 out): sampled outputs against the oracle,
+    element by element, including the corners of D and of its last tile.
+    bf16 rounding adds at most 2^-9 of the magnitude to the bound."""
+    M, N, K = 16384, 28672, 8192
+    fmt = E4M3
+    g = torch.Generator(device=DEV).manual_seed(4242)
+    codes = torch.from_numpy(_finite_codes(orc, fmt)).to(DEV)
+    qa = codes[torch.randint(0, len(codes), (M, K), device=DEV, generator=g)]
+    qb = codes[torch.randint(0, len(codes), (N, K), device=DEV, generator=g)]
+    sa = torch.exp(torch.randn((M, K // 128), device=DEV, generator=g) * 2.0 - 4.0)
+    sb = torch.exp(torch.randn((N // 128, K // 128), device=DEV, generator=g) * 2.0 - 6.0)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    gs.fp8_gemm_block_scaled(qa, sa, qb, sb, fmt, d)
+    torch.cuda.synchronize()
+    assert gs.gs_device_status() == 0
+    rng = np.random.default_rng(7)
+    ms = np.concatenate([[0, 0, M - 1, M - 1, M - 128, M - 1], rng.integers(0, M, 600)])
+    ns = np.concatenate([[0, N - 1, 0, N - 1, N - 128, N - 129], rng.integers(0, N, 600)])
+    qa_h = qa[torch.from_numpy(np.unique(ms)).to(DEV)].cpu().numpy()
+    row_of = {m: i for i, m in enumerate(np.unique(ms))}
+    sa_h = sa.cpu().numpy()
+    qb_h, sb_h = qb.cpu().numpy(), sb.cpu().numpy()
+    got = d[torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)].float().cpu().numpy()
+    nkb = K // 128
+    for i, (m, n) in enumerate(zip(ms, ns)):
+        a_row = np.ascontiguousarray(qa_h[row_of[m]][None, :])
+        s_row = np.ascontiguousarray(sa_h[m][None, :])
+        want = orc.gemm_fp8_block_elem(a_row, s_row, qb_h, sb_h, 0, int(n), fmt)
+        absd = orc.gemm_fp8_block_elem(a_row & 0x7F, s_row, qb_h & 0x7F, sb_h, 0, int(n), fmt)
+        tol = (2.0 ** -24 * (nkb + 3) + E_BLK) * absd
+        tol += 2.0 ** -8 * (abs(want) + tol)
+        assert abs(float(got[i]) - want) <= tol, (m, n, float(got[i]), want, tol)
