@@ -9,28 +9,30 @@
 //   D[m][n] = sum_kb sa[m][kb] * sb[n/128][kb] * sum_{k in kb} A[m][k] * B[n][k]
 //
 // A = [M, K] and B = [N, K] FP8 codes (both K-major, as fp8_quant_block
-// writes them), D = [M, N] fp32 or bf16.  One CTA per 128x128 tile of D,
-// warp-specialised:
-//   warp 0 (one lane)  TMA loads of 128x128-byte A and B tiles (128-byte
+// writes them), D = [M, N] fp32 or bf16.  Persistent CTAs (one per SM) walk
+// 128 x 256 tiles of D in groups of kGroupM tile rows (so the A and B panels
+// in use at once stay in L2); each CTA is warp-specialised:
+//   warp 0 (one lane)  TMA loads of the 128 x 128-byte A tile and the
+//                      256 x 128-byte B tile of each K-block (128-byte
 //                      swizzle, no multicast) into a 4-stage ring;
-//   warp 1             allocates 256 TMEM columns; one lane issues, per
+//   warp 1             allocates all 512 TMEM columns; one lane issues, per
 //                      128-wide K-block, four tcgen05.mma.kind::f8f6f4
-//                      (M 128, N 128, K 32) into one of two TMEM
+//                      (M 128, N 256, K 32) into one of two TMEM
 //                      accumulators, then commits to the stage's "empty"
 //                      barrier and the accumulator's "full" barrier;
-//   warps 2-5          read each block's 128x128 fp32 partial from TMEM
-//                      (tcgen05.ld, one row per thread), multiply by
-//                      sa * sb and add into fp32 registers (the promotion),
-//                      release the accumulator, and finally store D.
-// Every mbarrier wait is bounded by %globaltimer; a role that gives up sets
-// a shared abort flag and GS_ERR_TIMEOUT, the others leave their loops, the
-// MMA lane and the TMA lane wait (bounded) for their own work in flight, and
-// the TMEM columns are freed on every path.
+//   warps 2-9          each reads one 32-row x 128-column quarter of the
+//                      block's fp32 partial from TMEM (tcgen05.ld: warp w
+//                      sees TMEM lanes 32 (w % 4) ...), multiplies by
+//                      sa * sb and adds into fp32 registers (the
+//                      promotion), releases the accumulator, and after the
+//                      tile's last K-block stores its 32 x 128 piece of D
+//                      while the tensor cores already work on the next tile.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gs_device.cuh"
@@ -38,12 +40,17 @@
 
 namespace gs {
 
-constexpr int kGB = 128;                 // tile M = N = K-block
+constexpr int kGB = 128;                   // tile M, K-block, weight block
+constexpr int kGBN = 256;                  // tile N
 constexpr int kGStages = 4;
-constexpr int kGThreads = 192;
-constexpr int kGTile = kGB * kGB;        // bytes of one FP8 operand tile
-constexpr int kGTmemCols = 256;          // two 128-column fp32 accumulators
-constexpr int kGSmemBytes = 2 * kGStages * kGTile + 1024 + 256;
+constexpr int kGEpiWarps = 8;
+constexpr int kGThreads = 64 + 32 * kGEpiWarps;
+constexpr int kGTileA = kGB * kGB;         // bytes of one A stage
+constexpr int kGTileB = kGBN * kGB;        // bytes of one B stage
+constexpr int kGStageBytes = kGTileA + kGTileB;
+constexpr int kGTmemCols = 2 * kGBN;       // two 256-column fp32 accumulators
+constexpr int kGSmemBytes = kGStages * kGStageBytes + 1024 + 256;
+constexpr int kGroupM = 16;                // tile rows per raster group
 constexpr uint64_t kGWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t g_smem_u32(const void* p) {
@@ -118,9 +125,9 @@ __device__ __forceinline__ uint64_t umma_desc_k_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor of kind::f8f6f4: fp32 accumulator, A and B of the
-// given FP8 format (0 E4M3, 1 E5M2), both K-major, N = 128, M = 128.
+// given FP8 format (0 E4M3, 1 E5M2), both K-major, N = 256, M = 128.
 __host__ __device__ constexpr uint32_t umma_idesc_f8(uint32_t fmt) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kGB >> 3) << 17) |
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kGBN >> 3) << 17) |
          ((uint32_t)(kGB >> 4) << 24);
 }
 
@@ -158,6 +165,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Tile t of the raster -> (tile row, tile column), kGroupM tile rows at a
+// time so that consecutive tiles share A and B panels.
+__device__ __forceinline__ void gemm_tile_coords(int64_t t, int64_t tiles_m, int64_t tiles_n,
+                                                 int64_t& mt, int64_t& nt) {
+  const int64_t per_group = (int64_t)kGroupM * tiles_n;
+  const int64_t first_m = (t / per_group) * kGroupM;
+  const int64_t rows = min((int64_t)kGroupM, tiles_m - first_m);
+  const int64_t r = t % per_group;
+  mt = first_m + r % rows;
+  nt = r / rows;
+}
+
 template <int FMT, int OUT>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_fp8_block_scaled(const __grid_constant__ CUtensorMap map_a,
@@ -168,7 +187,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   // 1024-byte alignment of the swizzled tiles
   const uint32_t pad = (1024u - (g_smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* tiles = smem_raw + pad;
-  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + 2 * kGStages * kGTile);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + kGStages * kGStageBytes);
   uint64_t* empty = full + kGStages;
   uint64_t* tfull = empty + kGStages;
   uint64_t* tempty = tfull + 2;
@@ -177,8 +196,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n0 = (int64_t)blockIdx.x * kGB, m0 = (int64_t)blockIdx.y * kGB;
-  const int nkb = (int)((K + kGB - 1) / kGB);
+  const int nkb = (int)(K / kGB);
+  const int64_t tiles_m = (M + kGB - 1) / kGB, tiles_n = (N + kGBN - 1) / kGBN;
+  const int64_t n_tiles = tiles_m * tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGStages; ++s) {
@@ -187,7 +207,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       g_bar_init(&tfull[b], 1);
-      g_bar_init(&tempty[b], 128);
+      g_bar_init(&tempty[b], 32 * kGEpiWarps);
     }
     g_bar_init(drain, 1);
     *abort_flag = 0;
@@ -208,78 +228,105 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kGStages;
-        const uint32_t ph = (uint32_t)((kb / kGStages) & 1);
-        if (!g_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
-                         g_smem_u32(&full[s])),
-                     "r"(2 * kGTile)
-                     : "memory");
-        g_tma_load(&map_a, &full[s], tiles + s * kGTile, kb * kGB, (int32_t)m0);
-        g_tma_load(&map_b, &full[s], tiles + (kGStages + s) * kGTile, kb * kGB, (int32_t)n0);
-        ++issued;
+      int64_t it = 0;  // K-blocks issued so far, over all tiles of this CTA
+      bool go = true;
+      for (int64_t t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
+        int64_t mt, nt;
+        gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = (int)(it % kGStages);
+          const uint32_t ph = (uint32_t)((it / kGStages) & 1);
+          if (!g_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
+            go = false;
+            break;
+          }
+          uint8_t* st = tiles + s * kGStageBytes;
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                           g_smem_u32(&full[s])),
+                       "r"(kGStageBytes)
+                       : "memory");
+          g_tma_load(&map_a, &full[s], st, kb * kGB, (int32_t)(mt * kGB));
+          g_tma_load(&map_b, &full[s], st + kGTileA, kb * kGB, (int32_t)(nt * kGBN));
+        }
       }
       // Let the last load of every stage land before the CTA can exit (they
       // have landed already unless another role gave up).
-      for (int j = (issued > kGStages ? issued - kGStages : 0); j < issued; ++j)
+      for (int64_t j = (it > kGStages ? it - kGStages : 0); j < it; ++j)
         g_drain(&full[j % kGStages], (uint32_t)((j / kGStages) & 1));
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       constexpr uint32_t idesc = umma_idesc_f8((uint32_t)FMT);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kGStages, b = kb & 1;
-        const uint32_t ph = (uint32_t)((kb / kGStages) & 1), tph = (uint32_t)((kb >> 1) & 1);
-        if (!g_wait(&full[s], ph, abort_flag, status)) break;
-        if (!g_wait(&tempty[b], tph ^ 1u, abort_flag, status)) break;
-        tc_fence_after();
-        const uint32_t a0 = g_smem_u32(tiles + s * kGTile);
-        const uint32_t b0 = g_smem_u32(tiles + (kGStages + s) * kGTile);
+      int64_t it = 0;
+      bool go = true;
+      for (int64_t t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = (int)(it % kGStages), b = (int)(it & 1);
+          const uint32_t ph = (uint32_t)((it / kGStages) & 1), tph = (uint32_t)((it >> 1) & 1);
+          if (!g_wait(&full[s], ph, abort_flag, status) ||
+              !g_wait(&tempty[b], tph ^ 1u, abort_flag, status)) {
+            go = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = g_smem_u32(tiles + s * kGStageBytes);
+          const uint32_t b0 = a0 + kGTileA;
 #pragma unroll
-        for (int kk = 0; kk < kGB / 32; ++kk)
-          umma_f8(tmem + (uint32_t)(b * kGB), umma_desc_k_sw128(a0 + 32 * kk),
-                  umma_desc_k_sw128(b0 + 32 * kk), idesc, kk > 0 ? 1u : 0u);
-        umma_commit(&empty[s]);
-        umma_commit(&tfull[b]);
+          for (int kk = 0; kk < kGB / 32; ++kk)
+            umma_f8(tmem + (uint32_t)(b * kGBN), umma_desc_k_sw128(a0 + 32 * kk),
+                    umma_desc_k_sw128(b0 + 32 * kk), idesc, kk > 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+          umma_commit(&tfull[b]);
+        }
       }
       umma_commit(drain);  // completes when every MMA issued above has
       g_drain(drain, 0);
     }
-  } else {  // promotion and store: warps 2..5, one TMEM lane (row) per thread
-    const int q = warp & 3;
+  } else {  // promotion and store: warps 2..9
+    const int q = warp & 3;               // TMEM lane quarter this warp may read
+    const int h = (warp - 2) >> 2;        // which 128 columns of the 256
     const int row = 32 * q + lane;
-    const bool row_ok = m0 + row < M;  // rows past M were loaded as zeros
-    const float* sa_row = sa + (row_ok ? (m0 + row) * nkb : 0);
-    const float* sb_row = sb + (n0 / kGB) * nkb;
-    float acc[kGB];
+    int64_t it = 0;
+    bool go = true;
+    for (int64_t t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
+      int64_t mt, nt;
+      gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
+      const int64_t m = mt * kGB + row, n0 = nt * kGBN + h * kGB;
+      const bool live = m < M && n0 < N;  // rows / columns past the edge were zeros
+      const float* sa_row = sa + (live ? m * nkb : 0);
+      const float* sb_row = sb + (live ? (n0 / kGB) * nkb : 0);
+      float acc[kGB];
 #pragma unroll
-    for (int j = 0; j < kGB; ++j) acc[j] = 0.0f;
-    bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int b = kb & 1;
-      const uint32_t tph = (uint32_t)((kb >> 1) & 1);
-      // the warp leaves together: tcgen05.ld below needs all 32 lanes
-      const bool got = g_wait(&tfull[b], tph, abort_flag, status);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
+      for (int j = 0; j < kGB; ++j) acc[j] = 0.0f;
+      float sa_v = live ? sa_row[0] : 0.0f, sb_v = live ? sb_row[0] : 0.0f;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int b = (int)(it & 1);
+        const float sc = __fmul_rn(sa_v, sb_v);
+        if (live && kb + 1 < nkb) {  // next block's scales, ahead of the wait
+          sa_v = sa_row[kb + 1];
+          sb_v = sb_row[kb + 1];
+        }
+        // the warp leaves together: tcgen05.ld below needs all 32 lanes
+        const bool got = g_wait(&tfull[b], (uint32_t)((it >> 1) & 1), abort_flag, status);
+        if (!__all_sync(0xffffffffu, got)) {
+          go = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kGBN + h * kGB);
+#pragma unroll
+        for (int c = 0; c < kGB / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + 32 * c, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[32 * c + j] = __fmaf_rn(v[j], sc, acc[32 * c + j]);
+        }
+        tc_fence_before();
+        g_bar_arrive(&tempty[b]);
       }
-      tc_fence_after();
-      const float sc = row_ok ? __fmul_rn(sa_row[kb], sb_row[kb]) : 0.0f;
-#pragma unroll
-      for (int c = 0; c < kGB / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kGB + 32 * c), v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[32 * c + j] = __fmaf_rn(v[j], sc, acc[32 * c + j]);
-      }
-      tc_fence_before();
-      g_bar_arrive(&tempty[b]);
-    }
-    if (ok && !*abort_flag && row_ok) {
-      const int64_t off = (m0 + row) * N + n0;
+      if (!go || *abort_flag) break;
+      if (!live) continue;
+      const int64_t off = m * N + n0;
       if (vec_store && n0 + kGB <= N) {
         if constexpr (OUT == GS_F32) {
           float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(d) + off);
@@ -334,10 +381,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn() {
   return fn;
 }
 
-static CUresult encode_k_major(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K) {
+static CUresult encode_k_major(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K,
+                               uint32_t box_rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K};
-  const cuuint32_t box[2] = {kGB, kGB};
+  const cuuint32_t box[2] = {kGB, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return gemm_encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -356,7 +404,8 @@ static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const fl
     attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const dim3 grid((unsigned)((N + kGB - 1) / kGB), (unsigned)((M + kGB - 1) / kGB));
+  const int64_t tiles = ((M + kGB - 1) / kGB) * ((N + kGBN - 1) / kGBN);
+  const unsigned grid = (unsigned)std::min<int64_t>(tiles, (int64_t)sm_count());
   k<<<grid, kGThreads, kGSmemBytes, st>>>(ma, mb, sa, sb, M, N, K, vec_store, d, status);
   return cudaGetLastError();
 }
@@ -373,7 +422,8 @@ cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, con
   if (K == 0) return cudaMemsetAsync(d, 0, (size_t)M * (size_t)N * esz, st);  // empty sums
   if (!gemm_encode_fn()) return cudaErrorNotSupported;
   CUtensorMap ma, mb;
-  if (encode_k_major(&ma, qa, M, K) != CUDA_SUCCESS || encode_k_major(&mb, qb, N, K) != CUDA_SUCCESS)
+  if (encode_k_major(&ma, qa, M, K, kGB) != CUDA_SUCCESS ||
+      encode_k_major(&mb, qb, N, K, kGBN) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const int vec = (N % 8 == 0) && ((uintptr_t)d % 16 == 0);
   if (fmt == GS_E4M3)

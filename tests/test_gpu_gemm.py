@@ -9,6 +9,9 @@ Two kinds of case:
     order of the tensor cores' additions -- the result must equal the
     oracle bit for bit.  Any layout mistake (swizzle, K advance, operand
     transposed, wrong scale index, wrong TMEM lane) changes some value.
+    Shapes cover one tile, ragged M and N (partial tiles, an all-padding
+    half tile), more K-blocks than pipeline stages, and more tiles than
+    SMs in a partial raster group (the persistent loop).
   * general: every finite FP8 code and real-valued scales; the error against
     the exact sum must stay within
         tol = (2^-24 * (nkb + 3) + E_BLK) * sum_kb |sa sb| sum_k |a b|
@@ -100,7 +103,8 @@ def _assert_exact(orc, got, want_f64, out_dtype, what):
 
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (300, 200, 1280),
-                                   (1, 128, 128), (129, 1, 256), (130, 260, 640)])
+                                   (1, 128, 128), (129, 1, 256), (130, 260, 640),
+                                   (2048, 2560, 256), (2181, 2304, 128)])
 def test_gemm_exact_values_bit_exact(gs, orc, fmt, M, N, K):
     qa, sa, qb, sb = _exact_inputs(orc, fmt, M, N, K, seed=M * 7 + N * 3 + K + fmt)
     want = orc.gemm_fp8_block(qa, sa, qb, sb, fmt)
