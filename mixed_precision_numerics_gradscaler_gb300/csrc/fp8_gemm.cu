@@ -43,8 +43,18 @@ namespace gs {
 constexpr int kGB = 128;                   // tile M, K-block, weight block
 constexpr int kGBN = 256;                  // tile N
 constexpr int kGStages = 4;
-constexpr int kGEpiWarps = 8;
-constexpr int kGThreads = 64 + 32 * kGEpiWarps;
+constexpr int kGEpiWarps = 8;                    // warpgroups 1 and 2
+constexpr int kGThreads = 128 + 32 * kGEpiWarps;  // warpgroup 0: TMA, MMA, 2 idle
+// Register split (setmaxnreg): the CTA is launched with kGLaunchRegs per
+// thread (65536 / 384 rounded down to a multiple of 8); warpgroup 0 gives
+// back to kGCtrlRegs, warpgroups 1-2 grow to kGEpiRegs.  The shares must add
+// up to the launch total exactly or the growing warps would wait forever.
+constexpr int kGLaunchRegs = 168;
+constexpr int kGCtrlRegs = 40;
+constexpr int kGEpiRegs = 232;
+static_assert(4 * kGCtrlRegs + kGEpiWarps * kGEpiRegs <= (kGThreads / 32) * kGLaunchRegs,
+              "register split exceeds the launch allocation");
+static_assert(kGThreads * kGLaunchRegs <= 65536, "launch allocation exceeds the register file");
 constexpr int kGTileA = kGB * kGB;         // bytes of one A stage
 constexpr int kGTileB = kGBN * kGB;        // bytes of one B stage
 constexpr int kGStageBytes = kGTileA + kGTileB;
@@ -147,9 +157,9 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// 32 lanes x 32 consecutive fp32 columns of TMEM -> 32 registers per thread.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 32 lanes x 32 consecutive fp32 columns of TMEM -> 32 registers per thread
+// (asynchronous: the registers may be read only after tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -160,19 +170,48 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+// Waits for every tcgen05.ld of this thread; the registers of both loads are
+// passed through so that nothing reads them before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+        "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
+        "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]),
+        "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]),
+        "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]),
+        "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]),
+        "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]),
+        "+r"(b[14]), "+r"(b[15]), "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]),
+        "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]),
+        "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+      :
+      : "memory");
+}
+
+// Two fp32 lanes in one 64-bit register, for the packed fused multiply-add
+// (each lane is an IEEE fp32 fma, round to nearest even).
+__device__ __forceinline__ uint64_t f32x2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_fma(uint64_t& acc, uint64_t v, uint64_t s) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(v), "l"(s));
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
 }
 
 // Tile t of the raster -> (tile row, tile column), kGroupM tile rows at a
 // time so that consecutive tiles share A and B panels.
-__device__ __forceinline__ void gemm_tile_coords(int64_t t, int64_t tiles_m, int64_t tiles_n,
-                                                 int64_t& mt, int64_t& nt) {
-  const int64_t per_group = (int64_t)kGroupM * tiles_n;
-  const int64_t first_m = (t / per_group) * kGroupM;
-  const int64_t rows = min((int64_t)kGroupM, tiles_m - first_m);
-  const int64_t r = t % per_group;
+__device__ __forceinline__ void gemm_tile_coords(int t, int tiles_m, int tiles_n, int& mt,
+                                                 int& nt) {
+  const int per_group = kGroupM * tiles_n;
+  const int first_m = (t / per_group) * kGroupM;
+  const int rows = min(kGroupM, tiles_m - first_m);
+  const int r = t % per_group;
   mt = first_m + r % rows;
   nt = r / rows;
 }
@@ -197,8 +236,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (int)(K / kGB);
-  const int64_t tiles_m = (M + kGB - 1) / kGB, tiles_n = (N + kGBN - 1) / kGBN;
-  const int64_t n_tiles = tiles_m * tiles_n;
+  const int tiles_m = (int)((M + kGB - 1) / kGB), tiles_n = (int)((N + kGBN - 1) / kGBN);
+  const int n_tiles = tiles_m * tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGStages; ++s) {
@@ -226,16 +265,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {  // TMA producer
-      int64_t it = 0;  // K-blocks issued so far, over all tiles of this CTA
+  if (warp < 4) {  // warpgroup 0
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGCtrlRegs));
+    if (warp == 0 && lane == 0) {  // TMA producer
+      uint32_t it = 0;  // K-blocks issued so far over this CTA's tiles (mod 2^32)
       bool go = true;
-      for (int64_t t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
-        int64_t mt, nt;
+      for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
+        int mt, nt;
         gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = (int)(it % kGStages);
-          const uint32_t ph = (uint32_t)((it / kGStages) & 1);
+          const uint32_t s = it % kGStages, ph = (it / kGStages) & 1u;
           if (!g_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
             go = false;
             break;
@@ -245,24 +284,23 @@ __global__ void __launch_bounds__(kGThreads, 1)
                            g_smem_u32(&full[s])),
                        "r"(kGStageBytes)
                        : "memory");
-          g_tma_load(&map_a, &full[s], st, kb * kGB, (int32_t)(mt * kGB));
-          g_tma_load(&map_b, &full[s], st + kGTileA, kb * kGB, (int32_t)(nt * kGBN));
+          g_tma_load(&map_a, &full[s], st, kb * kGB, mt * kGB);
+          g_tma_load(&map_b, &full[s], st + kGTileA, kb * kGB, nt * kGBN);
         }
       }
       // Let the last load of every stage land before the CTA can exit (they
       // have landed already unless another role gave up).
-      for (int64_t j = (it > kGStages ? it - kGStages : 0); j < it; ++j)
-        g_drain(&full[j % kGStages], (uint32_t)((j / kGStages) & 1));
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer
+      const uint32_t issued_tail = it < kGStages ? it : kGStages;
+      for (uint32_t j = it - issued_tail; j != it; ++j)
+        g_drain(&full[j % kGStages], (j / kGStages) & 1u);
+    } else if (warp == 1 && lane == 0) {  // MMA issuer
       constexpr uint32_t idesc = umma_idesc_f8((uint32_t)FMT);
-      int64_t it = 0;
+      uint32_t it = 0;
       bool go = true;
-      for (int64_t t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
+      for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = (int)(it % kGStages), b = (int)(it & 1);
-          const uint32_t ph = (uint32_t)((it / kGStages) & 1), tph = (uint32_t)((it >> 1) & 1);
+          const uint32_t s = it % kGStages, b = it & 1u;
+          const uint32_t ph = (it / kGStages) & 1u, tph = (it >> 1) & 1u;
           if (!g_wait(&full[s], ph, abort_flag, status) ||
               !g_wait(&tempty[b], tph ^ 1u, abort_flag, status)) {
             go = false;
@@ -273,7 +311,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const uint32_t b0 = a0 + kGTileA;
 #pragma unroll
           for (int kk = 0; kk < kGB / 32; ++kk)
-            umma_f8(tmem + (uint32_t)(b * kGBN), umma_desc_k_sw128(a0 + 32 * kk),
+            umma_f8(tmem + b * kGBN, umma_desc_k_sw128(a0 + 32 * kk),
                     umma_desc_k_sw128(b0 + 32 * kk), idesc, kk > 0 ? 1u : 0u);
           umma_commit(&empty[s]);
           umma_commit(&tfull[b]);
@@ -282,44 +320,51 @@ __global__ void __launch_bounds__(kGThreads, 1)
       umma_commit(drain);  // completes when every MMA issued above has
       g_drain(drain, 0);
     }
-  } else {  // promotion and store: warps 2..9
+  } else {  // promotion and store: warpgroups 1 and 2
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGEpiRegs));
     const int q = warp & 3;               // TMEM lane quarter this warp may read
-    const int h = (warp - 2) >> 2;        // which 128 columns of the 256
+    const int h = (warp - 4) >> 2;        // which 128 columns of the 256
     const int row = 32 * q + lane;
-    int64_t it = 0;
+    uint32_t it = 0;
     bool go = true;
-    for (int64_t t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
-      int64_t mt, nt;
+    for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
+      int mt, nt;
       gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
-      const int64_t m = mt * kGB + row, n0 = nt * kGBN + h * kGB;
+      const int64_t m = (int64_t)mt * kGB + row, n0 = (int64_t)nt * kGBN + h * kGB;
       const bool live = m < M && n0 < N;  // rows / columns past the edge were zeros
       const float* sa_row = sa + (live ? m * nkb : 0);
       const float* sb_row = sb + (live ? (n0 / kGB) * nkb : 0);
-      float acc[kGB];
+      uint64_t acc[kGB / 2];  // column pairs (2j, 2j + 1)
 #pragma unroll
-      for (int j = 0; j < kGB; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < kGB / 2; ++j) acc[j] = 0ull;
       float sa_v = live ? sa_row[0] : 0.0f, sb_v = live ? sb_row[0] : 0.0f;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int b = (int)(it & 1);
+        const uint32_t b = it & 1u;
         const float sc = __fmul_rn(sa_v, sb_v);
+        const uint64_t sc2 = f32x2_pack(__float_as_uint(sc), __float_as_uint(sc));
         if (live && kb + 1 < nkb) {  // next block's scales, ahead of the wait
           sa_v = sa_row[kb + 1];
           sb_v = sb_row[kb + 1];
         }
         // the warp leaves together: tcgen05.ld below needs all 32 lanes
-        const bool got = g_wait(&tfull[b], (uint32_t)((it >> 1) & 1), abort_flag, status);
+        const bool got = g_wait(&tfull[b], (it >> 1) & 1u, abort_flag, status);
         if (!__all_sync(0xffffffffu, got)) {
           go = false;
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kGBN + h * kGB);
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + b * kGBN + h * kGB;
 #pragma unroll
-        for (int c = 0; c < kGB / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + 32 * c, v);
+        for (int c = 0; c < kGB / 32; c += 2) {  // 64 columns per wait
+          uint32_t v0[32], v1[32];
+          tmem_ld32(taddr + 32 * c, v0);
+          tmem_ld32(taddr + 32 * (c + 1), v1);
+          tmem_wait_ld(v0, v1);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[32 * c + j] = __fmaf_rn(v[j], sc, acc[32 * c + j]);
+          for (int j = 0; j < 16; ++j) {
+            f32x2_fma(acc[16 * c + j], f32x2_pack(v0[2 * j], v0[2 * j + 1]), sc2);
+            f32x2_fma(acc[16 * c + 16 + j], f32x2_pack(v1[2 * j], v1[2 * j + 1]), sc2);
+          }
         }
         tc_fence_before();
         g_bar_arrive(&tempty[b]);
@@ -327,30 +372,33 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (!go || *abort_flag) break;
       if (!live) continue;
       const int64_t off = m * N + n0;
+      float out[kGB];
+#pragma unroll
+      for (int j = 0; j < kGB / 2; ++j) f32x2_unpack(acc[j], out[2 * j], out[2 * j + 1]);
       if (vec_store && n0 + kGB <= N) {
         if constexpr (OUT == GS_F32) {
           float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(d) + off);
 #pragma unroll
           for (int j = 0; j < kGB / 4; ++j)
-            dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+            dst[j] = make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
         } else {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(d) + off);
 #pragma unroll
           for (int j = 0; j < kGB / 8; ++j)
-            dst[j] = make_uint4(cvt_f32x2_bf16x2(acc[8 * j + 1], acc[8 * j]),
-                                cvt_f32x2_bf16x2(acc[8 * j + 3], acc[8 * j + 2]),
-                                cvt_f32x2_bf16x2(acc[8 * j + 5], acc[8 * j + 4]),
-                                cvt_f32x2_bf16x2(acc[8 * j + 7], acc[8 * j + 6]));
+            dst[j] = make_uint4(cvt_f32x2_bf16x2(out[8 * j + 1], out[8 * j]),
+                                cvt_f32x2_bf16x2(out[8 * j + 3], out[8 * j + 2]),
+                                cvt_f32x2_bf16x2(out[8 * j + 5], out[8 * j + 4]),
+                                cvt_f32x2_bf16x2(out[8 * j + 7], out[8 * j + 6]));
         }
       } else {  // ragged N or unaligned D: one element at a time
 #pragma unroll
         for (int j = 0; j < kGB; ++j) {
           if (n0 + j < N) {
             if constexpr (OUT == GS_F32)
-              reinterpret_cast<float*>(d)[off + j] = acc[j];
+              reinterpret_cast<float*>(d)[off + j] = out[j];
             else
               reinterpret_cast<uint16_t*>(d)[off + j] =
-                  (uint16_t)(cvt_f32x2_bf16x2(0.0f, acc[j]) & 0xFFFFu);
+                  (uint16_t)(cvt_f32x2_bf16x2(0.0f, out[j]) & 0xFFFFu);
           }
         }
       }
@@ -402,6 +450,12 @@ static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const fl
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
+    // The setmaxnreg split is sized for exactly kGLaunchRegs per thread at
+    // launch; a build that allocated another count must not run.
+    cudaFuncAttributes fa;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, k);
+    if (attr_err == cudaSuccess && fa.numRegs != kGLaunchRegs)
+      attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = ((M + kGB - 1) / kGB) * ((N + kGBN - 1) / kGBN);
