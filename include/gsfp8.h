@@ -331,7 +331,7 @@ int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C
  *   fmt: GS_E4M3 or GS_E5M2, the format of both operands;
  *   d: row-major [M, N], out_dtype GS_F32 or GS_BF16 (rounded to nearest
  *      even from the fp32 sum).
- * K % 128 == 0, M, N, K < 2^31 and fewer than 2^31 tiles of 128 x 256
+ * K % 128 == 0, M, N, K < 2^31 and fewer than 2^30 tiles of 128 x 256
  * (else GS_ERR_SHAPE); M and N need not be multiples of 128; K == 0 writes
  * zeros.  qa and qb must be 16-byte
  * aligned (they are read by TMA; else GS_ERR_ARG).  Accuracy against the

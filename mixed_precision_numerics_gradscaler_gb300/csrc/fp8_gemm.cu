@@ -9,37 +9,32 @@
 //   D[m][n] = sum_kb sa[m][kb] * sb[n/128][kb] * sum_{k in kb} A[m][k] * B[n][k]
 //
 // A = [M, K] and B = [N, K] FP8 codes (both K-major, as fp8_quant_block
-// writes them), D = [M, N] fp32 or bf16.  Clusters of two CTAs (one per
-// SM) walk 256 x 256 tiles of D; the pair computes each K-block with the
-// 2-SM form of the MMA (tcgen05.mma.cta_group::2, M 256, N 256, K 32): each
-// CTA stages only its own 128 rows of A and its own 128 rows of B, so a
-// K-block costs each SM 32 KB of loads instead of the 48 KB a one-SM
-// 128 x 256 tile needs.  Each CTA is warp-specialised:
-//   warp 0 (one lane)  TMA loads of its A and B halves (128-byte swizzle,
-//                      no multicast) into a 6-stage ring; completion is
-//                      counted on the first CTA's barrier;
-//   warp 1             allocates all 512 TMEM columns (both CTAs); in the
-//                      first CTA one lane issues four MMAs per K-block into
-//                      one of two 256-column accumulators and commits to
-//                      both CTAs' "empty" and "full" barriers;
-//   warps 4-11         each reads a 32-row x 128-column quarter of the
-//                      CTA's 128 x 256 partial from TMEM (warp w sees TMEM
-//                      lanes 32 (w % 4) ...), multiplies by sa * sb and adds
-//                      into fp32 registers (packed fp32x2 fma: the
-//                      promotion), releases the accumulator to the first
-//                      CTA, and after the tile's last K-block stores its
-//                      32 x 128 piece of D while the next tile is computed.
-// Every mbarrier wait is bounded by %globaltimer; a role that gives up sets
-// a shared abort flag and GS_ERR_TIMEOUT, the others leave their loops, the
-// MMA lane and the TMA lane wait (bounded) for their own work in flight,
-// both CTAs meet at a cluster barrier, and the TMEM columns are freed on
-// every path.
+// writes them), D = [M, N] fp32 or bf16.  Persistent CTAs (one per SM) walk
+// 128 x 256 tiles of D in groups of kGroupM tile rows (so the A and B panels
+// in use at once stay in L2); each CTA is warp-specialised:
+//   warp 0 (one lane)  TMA loads of the 128 x 128-byte A tile and the
+//                      256 x 128-byte B tile of each K-block (128-byte
+//                      swizzle, no multicast) into a 4-stage ring;
+//   warp 1             allocates all 512 TMEM columns; one lane issues, per
+//                      128-wide K-block, four tcgen05.mma.kind::f8f6f4
+//                      (M 128, N 256, K 32) into one of two TMEM
+//                      accumulators, then commits to the stage's "empty"
+//                      barrier and the accumulator's "full" barrier;
+//   warps 2-9          each reads one 32-row x 128-column quarter of the
+//                      block's fp32 partial from TMEM (tcgen05.ld: warp w
+//                      sees TMEM lanes 32 (w % 4) ...), multiplies by
+//                      sa * sb and adds into fp32 registers (packed fp32x2
+//                      fma: the promotion), releasing the accumulator as
+//                      soon as its last TMEM read completes; after the
+//                      tile's last K-block it stores its 32 x 128 piece of D
+//                      while the tensor cores already work on the next tile.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "gs_device.cuh"
@@ -47,10 +42,9 @@
 
 namespace gs {
 
-constexpr int kGB = 128;                   // K-block, weight block, rows per CTA
-constexpr int kGBM = 256;                  // tile rows (the CTA pair)
-constexpr int kGBN = 256;                  // tile columns
-constexpr int kGStages = 6;
+constexpr int kGB = 128;                   // tile M, K-block, weight block
+constexpr int kGBN = 256;                  // tile N
+constexpr int kGStages = 4;
 constexpr int kGEpiWarps = 8;                    // warpgroups 1 and 2
 constexpr int kGThreads = 128 + 32 * kGEpiWarps;  // warpgroup 0: TMA, MMA, 2 idle
 // Register split (setmaxnreg): the CTA is launched with kGLaunchRegs per
@@ -63,16 +57,14 @@ constexpr int kGEpiRegs = 232;
 static_assert(4 * kGCtrlRegs + kGEpiWarps * kGEpiRegs <= (kGThreads / 32) * kGLaunchRegs,
               "register split exceeds the launch allocation");
 static_assert(kGThreads * kGLaunchRegs <= 65536, "launch allocation exceeds the register file");
-constexpr int kGTileA = kGB * kGB;         // this CTA's 128 rows of A, one K-block
-constexpr int kGTileB = kGB * kGB;         // this CTA's 128 rows of B, one K-block
+constexpr int kGTileA = kGB * kGB;         // bytes of one A stage
+constexpr int kGTileB = kGBN * kGB;        // bytes of one B stage
 constexpr int kGStageBytes = kGTileA + kGTileB;
 constexpr int kGTmemCols = 2 * kGBN;       // two 256-column fp32 accumulators
-// Stages, barriers, 1024-byte alignment slack, and one spare B tile so that
-// no operand descriptor of the last stage can reach past the allocation.
-constexpr int kGSmemBytes = kGStages * kGStageBytes + 1024 + 256 + kGTileB;
+constexpr int kGOutBytes = 32 * 128;      // per promotion warp: 32 rows x 128 bytes of D
+constexpr int kGSmemBytes = kGStages * kGStageBytes + kGEpiWarps * kGOutBytes + 1024 + 256;
 static_assert(kGSmemBytes <= 232448, "dynamic shared memory above the per-CTA limit");
-constexpr uint32_t kGReleases = 2 * kGEpiWarps;  // promotion warps of the pair
-constexpr int kGroupM = 8;                 // tile rows per raster group
+constexpr int kGroupM = 16;                // tile rows per raster group
 constexpr uint64_t kGWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t g_smem_u32(const void* p) {
@@ -119,39 +111,23 @@ __device__ __forceinline__ void g_drain(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ void g_bar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(g_smem_u32(bar)), "r"(count) : "memory");
 }
-// Arrival on a barrier given by its shared::cluster address (this CTA's or
-// the peer's).  The promotion warps signal with it that their TMEM reads are
-// done (ordered by tcgen05.wait::ld and tcgen05.fence::before_thread_sync);
-// no global or shared data is handed over, so the default CTA-scope
-// semantics suffice -- a cluster-scope release would make every signal wait
-// for the thread's outstanding stores of D.
-__device__ __forceinline__ void g_bar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+__device__ __forceinline__ void g_bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(g_smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ uint32_t g_cta_rank() {
-  uint32_t r;
-  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// shared::cluster address of the same shared-memory offset in CTA `rank`.
-__device__ __forceinline__ uint32_t g_map_rank(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(g_smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void g_cluster_sync() {
+__device__ __forceinline__ void g_tma_load(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                           int32_t x, int32_t y) {
   asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// TMA tile load into this CTA's shared memory, its byte count completed on
-// the barrier at `bar_cluster` (in either CTA of the pair).
-__device__ __forceinline__ void g_tma_load_2sm(const CUtensorMap* map, uint32_t bar_cluster,
-                                               void* dst, int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(g_smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(bar_cluster)
+      "l"(map), "r"(x), "r"(y), "r"(g_smem_u32(bar))
+      : "memory");
+}
+// TMA tile store from this CTA's shared memory (bulk-group completion).
+__device__ __forceinline__ void g_tma_store(const CUtensorMap* map, const void* src, int32_t x,
+                                            int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+      "r"(x), "r"(y), "r"(g_smem_u32(src))
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -171,38 +147,24 @@ __device__ __forceinline__ uint64_t umma_desc_k_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor of kind::f8f6f4: fp32 accumulator, A and B of the
-// given FP8 format (0 E4M3, 1 E5M2), both K-major, N = 256, M = 256 (the
-// pair: 128 rows in each CTA's TMEM).
+// given FP8 format (0 E4M3, 1 E5M2), both K-major, N = 256, M = 128.
 __host__ __device__ constexpr uint32_t umma_idesc_f8(uint32_t fmt) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kGBN >> 3) << 17) |
-         ((uint32_t)(kGBM >> 4) << 24);
+         ((uint32_t)(kGB >> 4) << 24);
 }
 
-// D[tmem] (+)= A[adesc] * B[bdesc]^T over both CTAs of the pair: A's rows
-// 0-127 and B's rows 0-127 come from this CTA's shared memory at the
-// descriptors' addresses, rows 128-255 from the peer's at the same offsets.
-__device__ __forceinline__ void umma_f8_2sm(uint32_t tmem_d, uint64_t a, uint64_t b,
-                                            uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_f8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive once on the barrier at this offset in both CTAs when every MMA
-// issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(g_smem_u32(bar)),
-      "h"((uint16_t)0x3)
-      : "memory");
-}
-// Same, on this CTA's barrier only.
-__device__ __forceinline__ void umma_commit_local(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           g_smem_u32(bar))
       : "memory");
 }
@@ -266,17 +228,19 @@ __device__ __forceinline__ void gemm_tile_coords(int t, int tiles_m, int tiles_n
   nt = r / rows;
 }
 
-template <int FMT, int OUT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
+template <int FMT, int OUT, bool TMA_STORE>
+__global__ void __launch_bounds__(kGThreads, 1)
     gemm_fp8_block_scaled(const __grid_constant__ CUtensorMap map_a,
-                          const __grid_constant__ CUtensorMap map_b, const float* __restrict__ sa,
+                          const __grid_constant__ CUtensorMap map_b,
+                          const __grid_constant__ CUtensorMap map_d, const float* __restrict__ sa,
                           const float* __restrict__ sb, int64_t M, int64_t N, int64_t K,
-                          int vec_store, void* __restrict__ d, int32_t* status) {
+                          void* __restrict__ d, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment of the swizzled tiles (the same offsets in both CTAs)
+  // 1024-byte alignment of the swizzled tiles
   const uint32_t pad = (1024u - (g_smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* tiles = smem_raw + pad;
-  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + kGStages * kGStageBytes);
+  uint8_t* out_stage = tiles + kGStages * kGStageBytes;  // 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + kGEpiWarps * kGOutBytes);
   uint64_t* empty = full + kGStages;
   uint64_t* tfull = empty + kGStages;
   uint64_t* tempty = tfull + 2;
@@ -285,10 +249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = g_cta_rank();  // 0 issues the MMAs; 1 is its peer
-  const int pair = (int)(blockIdx.x >> 1), n_pairs = (int)(gridDim.x >> 1);
   const int nkb = (int)(K / kGB);
-  const int tiles_m = (int)((M + kGBM - 1) / kGBM), tiles_n = (int)((N + kGBN - 1) / kGBN);
+  const int tiles_m = (int)((M + kGB - 1) / kGB), tiles_n = (int)((N + kGBN - 1) / kGBN);
   const int n_tiles = tiles_m * tiles_n;
 
   if (threadIdx.x == 0) {
@@ -298,33 +260,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       g_bar_init(&tfull[b], 1);
-      g_bar_init(&tempty[b], kGReleases);
+      g_bar_init(&tempty[b], 32 * kGEpiWarps);
     }
     g_bar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {  // both CTAs allocate together
+  if (warp == 1) {
     __syncwarp();
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      g_smem_u32(tmem_slot)),
                  "r"(kGTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  __syncwarp();
   tc_fence_before();
-  g_cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {  // warpgroup 0
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGCtrlRegs));
-    if (warp == 0 && lane == 0) {  // TMA producer (both CTAs)
-      const uint32_t full_lead = g_map_rank(full, 0);
+    if (warp == 0 && lane == 0) {  // TMA producer
       uint32_t it = 0;  // K-blocks issued so far over this CTA's tiles (mod 2^32)
       bool go = true;
-      for (int t = pair; go && t < n_tiles; t += n_pairs) {
+      for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
         int mt, nt;
         gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -334,29 +294,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
             break;
           }
           uint8_t* st = tiles + s * kGStageBytes;
-          if (rank == 0)  // the first CTA's barrier counts both CTAs' bytes
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
-                             g_smem_u32(&full[s])),
-                         "r"(2 * kGStageBytes)
-                         : "memory");
-          g_tma_load_2sm(&map_a, full_lead + 8 * s, st, kb * kGB, mt * kGBM + (int)rank * kGB);
-          g_tma_load_2sm(&map_b, full_lead + 8 * s, st + kGTileA, kb * kGB,
-                         nt * kGBN + (int)rank * kGB);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                           g_smem_u32(&full[s])),
+                       "r"(kGStageBytes)
+                       : "memory");
+          g_tma_load(&map_a, &full[s], st, kb * kGB, mt * kGB);
+          g_tma_load(&map_b, &full[s], st + kGTileA, kb * kGB, nt * kGBN);
         }
       }
       // Let the last load of every stage land before the CTA can exit (they
-      // have landed already unless another role gave up).  Only the first
-      // CTA's barriers see the completions.
-      if (rank == 0) {
-        const uint32_t tail = it < kGStages ? it : kGStages;
-        for (uint32_t j = it - tail; j != it; ++j)
-          g_drain(&full[j % kGStages], (j / kGStages) & 1u);
-      }
-    } else if (warp == 1 && lane == 0 && rank == 0) {  // MMA issuer
+      // have landed already unless another role gave up).
+      const uint32_t issued_tail = it < kGStages ? it : kGStages;
+      for (uint32_t j = it - issued_tail; j != it; ++j)
+        g_drain(&full[j % kGStages], (j / kGStages) & 1u);
+    } else if (warp == 1 && lane == 0) {  // MMA issuer
       constexpr uint32_t idesc = umma_idesc_f8((uint32_t)FMT);
       uint32_t it = 0;
       bool go = true;
-      for (int t = pair; go && t < n_tiles; t += n_pairs) {
+      for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const uint32_t s = it % kGStages, b = it & 1u;
           const uint32_t ph = (it / kGStages) & 1u, tph = (it >> 1) & 1u;
@@ -370,35 +325,103 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           const uint32_t b0 = a0 + kGTileA;
 #pragma unroll
           for (int kk = 0; kk < kGB / 32; ++kk)
-            umma_f8_2sm(tmem + b * kGBN, umma_desc_k_sw128(a0 + 32 * kk),
-                        umma_desc_k_sw128(b0 + 32 * kk), idesc, kk > 0 ? 1u : 0u);
-          umma_commit_pair(&empty[s]);
-          umma_commit_pair(&tfull[b]);
+            umma_f8(tmem + b * kGBN, umma_desc_k_sw128(a0 + 32 * kk),
+                    umma_desc_k_sw128(b0 + 32 * kk), idesc, kk > 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+          umma_commit(&tfull[b]);
         }
       }
-      umma_commit_local(drain);  // completes when every MMA issued above has
+      umma_commit(drain);  // completes when every MMA issued above has
       g_drain(drain, 0);
     }
-  } else {  // promotion and store: warpgroups 1 and 2 (both CTAs)
+  } else {  // promotion and store: warpgroups 1 and 2
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGEpiRegs));
     const int q = warp & 3;               // TMEM lane quarter this warp may read
     const int h = (warp - 4) >> 2;        // which 128 columns of the 256
     const int row = 32 * q + lane;
-    const uint32_t tempty_lead = g_map_rank(tempty, 0);
+    // Store this thread's 128 promoted values of row m, columns n0.. of D.
+    // TMA path (all 32 lanes call it): each 128-byte column chunk of the
+    // warp's 32 rows is written to its staging buffer in the 128-byte
+    // swizzled layout (16-byte piece p of row r at p ^ (r % 8)) and stored
+    // by one TMA instruction, which also clips rows and columns past D.
+    uint8_t* const my_out = out_stage + (warp - 4) * kGOutBytes;
+    auto store_tile = [&](int64_t m, int64_t n0, bool live, const uint64_t (&acc)[kGB / 2]) {
+      if constexpr (TMA_STORE) {
+        if (!__any_sync(0xffffffffu, live)) return;
+        constexpr int kCols = OUT == GS_F32 ? 32 : 64;  // columns per 128-byte chunk
+#pragma unroll
+        for (int c = 0; c < kGB / kCols; ++c) {
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();  // the previous chunk has been read out of the buffer
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            float o[8];  // this 16-byte piece's values (4 fp32 or 8 bf16)
+#pragma unroll
+            for (int j = 0; j < (OUT == GS_F32 ? 2 : 4); ++j)
+              f32x2_unpack(acc[c * kCols / 2 + (OUT == GS_F32 ? 2 : 4) * p + j], o[2 * j],
+                           o[2 * j + 1]);
+            uint4 v;
+            if constexpr (OUT == GS_F32)
+              v = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                             __float_as_uint(o[3]));
+            else
+              v = make_uint4(cvt_f32x2_bf16x2(o[1], o[0]), cvt_f32x2_bf16x2(o[3], o[2]),
+                             cvt_f32x2_bf16x2(o[5], o[4]), cvt_f32x2_bf16x2(o[7], o[6]));
+            *reinterpret_cast<uint4*>(my_out + lane * 128 + ((p ^ (lane & 7)) << 4)) = v;
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            g_tma_store(&map_d, my_out, (int32_t)(n0 + c * kCols), (int32_t)(m - lane));
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
+      } else {  // unaligned D or row stride: one element at a time
+        if (!live) return;
+        const int64_t off = m * N + n0;
+#pragma unroll
+        for (int j = 0; j < kGB / 2; ++j) {
+          float lo, hi;
+          f32x2_unpack(acc[j], lo, hi);
+          if constexpr (OUT == GS_F32) {
+            if (n0 + 2 * j < N) reinterpret_cast<float*>(d)[off + 2 * j] = lo;
+            if (n0 + 2 * j + 1 < N) reinterpret_cast<float*>(d)[off + 2 * j + 1] = hi;
+          } else {
+            const uint32_t pr = cvt_f32x2_bf16x2(hi, lo);
+            if (n0 + 2 * j < N) reinterpret_cast<uint16_t*>(d)[off + 2 * j] = (uint16_t)(pr & 0xFFFFu);
+            if (n0 + 2 * j + 1 < N) reinterpret_cast<uint16_t*>(d)[off + 2 * j + 1] = (uint16_t)(pr >> 16);
+          }
+        }
+      }
+    };
+    // This thread's row and column block of tile t, and its scale rows.
+    auto locate = [&](int t, int64_t& m, int64_t& n0, bool& live, const float*& sa_row,
+                      const float*& sb_row) {
+      int mt = 0, nt = 0;
+      if (t < n_tiles) gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
+      m = (int64_t)mt * kGB + row;
+      n0 = (int64_t)nt * kGBN + h * kGB;
+      live = t < n_tiles && m < M && n0 < N;  // rows / columns past the edge were zeros
+      sa_row = sa + (live ? m * nkb : 0);
+      sb_row = sb + (live ? (n0 / kGB) * nkb : 0);
+    };
+    int64_t m, n0;
+    bool live;
+    const float *sa_row, *sb_row;
+    locate(blockIdx.x, m, n0, live, sa_row, sb_row);
+    float sa_v = live ? sa_row[0] : 0.0f, sb_v = live ? sb_row[0] : 0.0f;
+    const int kb_ahead = nkb > 4 ? nkb - 4 : 0;  // when to fetch the next tile's first scales
     uint32_t it = 0;
     bool go = true;
-    for (int t = pair; go && t < n_tiles; t += n_pairs) {
-      int mt, nt;
-      gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
-      const int64_t m = (int64_t)mt * kGBM + (int64_t)rank * kGB + row;
-      const int64_t n0 = (int64_t)nt * kGBN + h * kGB;
-      const bool live = m < M && n0 < N;  // rows / columns past the edge were zeros
-      const float* sa_row = sa + (live ? m * nkb : 0);
-      const float* sb_row = sb + (live ? (n0 / kGB) * nkb : 0);
+    for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
+      int64_t m_n, n0_n;
+      bool live_n;
+      const float *sa_row_n, *sb_row_n;
+      locate(t + gridDim.x, m_n, n0_n, live_n, sa_row_n, sb_row_n);
+      float sa_first_n = 0.0f, sb_first_n = 0.0f;
       uint64_t acc[kGB / 2];  // column pairs (2j, 2j + 1)
 #pragma unroll
       for (int j = 0; j < kGB / 2; ++j) acc[j] = 0ull;
-      float sa_v = live ? sa_row[0] : 0.0f, sb_v = live ? sb_row[0] : 0.0f;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const uint32_t b = it & 1u;
         const float sc = __fmul_rn(sa_v, sb_v);
@@ -406,6 +429,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         if (live && kb + 1 < nkb) {  // next block's scales, ahead of the wait
           sa_v = sa_row[kb + 1];
           sb_v = sb_row[kb + 1];
+        }
+        if (kb == kb_ahead && live_n) {  // the next tile's, well ahead of its start
+          sa_first_n = sa_row_n[0];
+          sb_first_n = sb_row_n[0];
         }
         // the warp leaves together: tcgen05.ld below needs all 32 lanes
         const bool got = g_wait(&tfull[b], (it >> 1) & 1u, abort_flag, status);
@@ -415,67 +442,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + b * kGBN + h * kGB;
+        uint32_t v0[32], v1[32];  // 64 columns per wait
+        tmem_ld32(taddr, v0);
+        tmem_ld32(taddr + 32, v1);
+        tmem_wait_ld(v0, v1);
 #pragma unroll
-        for (int c = 0; c < kGB / 32; c += 2) {  // 64 columns per wait
-          uint32_t v0[32], v1[32];
-          tmem_ld32(taddr + 32 * c, v0);
-          tmem_ld32(taddr + 32 * (c + 1), v1);
-          tmem_wait_ld(v0, v1);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            f32x2_fma(acc[16 * c + j], f32x2_pack(v0[2 * j], v0[2 * j + 1]), sc2);
-            f32x2_fma(acc[16 * c + 16 + j], f32x2_pack(v1[2 * j], v1[2 * j + 1]), sc2);
-          }
+        for (int j = 0; j < 16; ++j) {
+          f32x2_fma(acc[j], f32x2_pack(v0[2 * j], v0[2 * j + 1]), sc2);
+          f32x2_fma(acc[16 + j], f32x2_pack(v1[2 * j], v1[2 * j + 1]), sc2);
         }
+        tmem_ld32(taddr + 64, v0);
+        tmem_ld32(taddr + 96, v1);
+        tmem_wait_ld(v0, v1);
+        // Every TMEM read of this block is done: hand the accumulator back
+        // to the MMA before the last FMAs.
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) g_bar_arrive_cluster(tempty_lead + 8 * b);
+        g_bar_arrive(&tempty[b]);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          f32x2_fma(acc[32 + j], f32x2_pack(v0[2 * j], v0[2 * j + 1]), sc2);
+          f32x2_fma(acc[48 + j], f32x2_pack(v1[2 * j], v1[2 * j + 1]), sc2);
+        }
       }
       if (!go || *abort_flag) break;
-      if (!live) continue;
-      const int64_t off = m * N + n0;
-      float out[kGB];
-#pragma unroll
-      for (int j = 0; j < kGB / 2; ++j) f32x2_unpack(acc[j], out[2 * j], out[2 * j + 1]);
-      if (vec_store && n0 + kGB <= N) {
-        if constexpr (OUT == GS_F32) {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(d) + off);
-#pragma unroll
-          for (int j = 0; j < kGB / 4; ++j)
-            dst[j] = make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(d) + off);
-#pragma unroll
-          for (int j = 0; j < kGB / 8; ++j)
-            dst[j] = make_uint4(cvt_f32x2_bf16x2(out[8 * j + 1], out[8 * j]),
-                                cvt_f32x2_bf16x2(out[8 * j + 3], out[8 * j + 2]),
-                                cvt_f32x2_bf16x2(out[8 * j + 5], out[8 * j + 4]),
-                                cvt_f32x2_bf16x2(out[8 * j + 7], out[8 * j + 6]));
-        }
-      } else {  // ragged N or unaligned D: one element at a time
-#pragma unroll
-        for (int j = 0; j < kGB; ++j) {
-          if (n0 + j < N) {
-            if constexpr (OUT == GS_F32)
-              reinterpret_cast<float*>(d)[off + j] = out[j];
-            else
-              reinterpret_cast<uint16_t*>(d)[off + j] =
-                  (uint16_t)(cvt_f32x2_bf16x2(0.0f, out[j]) & 0xFFFFu);
-          }
-        }
-      }
+      store_tile(m, n0, live, acc);
+      m = m_n;
+      n0 = n0_n;
+      live = live_n;
+      sa_row = sa_row_n;
+      sb_row = sb_row_n;
+      sa_v = sa_first_n;
+      sb_v = sb_first_n;
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // D written
   }
-  // Neither CTA leaves (or frees TMEM) while the pair's MMAs may still read
-  // its shared memory or write its TMEM: the first CTA's MMA lane has
-  // drained, every promotion warp has finished its reads.
-  __syncwarp();
   tc_fence_before();
-  g_cluster_sync();
+  __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kGTmemCols)
                  : "memory");
   }
@@ -507,14 +513,13 @@ static CUresult encode_k_major(CUtensorMap* map, const uint8_t* base, int64_t ro
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int FMT, int OUT>
-static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const float* sa,
-                          const float* sb, int64_t M, int64_t N, int64_t K, int vec_store,
+template <int FMT, int OUT, bool TMA_STORE>
+static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                          const float* sa, const float* sb, int64_t M, int64_t N, int64_t K,
                           void* d, int32_t* status, cudaStream_t st) {
-  auto k = gemm_fp8_block_scaled<FMT, OUT>;
+  auto k = gemm_fp8_block_scaled<FMT, OUT, TMA_STORE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  static int max_pairs = 0;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
     // The setmaxnreg split is sized for exactly kGLaunchRegs per thread at
@@ -523,24 +528,16 @@ static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const fl
     if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, k);
     if (attr_err == cudaSuccess && fa.numRegs != kGLaunchRegs)
       attr_err = cudaErrorInvalidConfiguration;
-    if (attr_err == cudaSuccess) {  // CTA pairs that can be resident at once
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (unsigned)sm_count(), 1, 1);
-      cfg.blockDim = dim3(kGThreads, 1, 1);
-      cfg.dynamicSmemBytes = kGSmemBytes;
-      attr_err = cudaOccupancyMaxActiveClusters(&max_pairs, (void*)k, &cfg);
-      if (attr_err == cudaSuccess && max_pairs < 1) attr_err = cudaErrorInvalidConfiguration;
-    }
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int64_t tiles = ((M + kGBM - 1) / kGBM) * ((N + kGBN - 1) / kGBN);
-  const unsigned pairs = (unsigned)std::min<int64_t>(tiles, (int64_t)max_pairs);
-  k<<<2 * pairs, kGThreads, kGSmemBytes, st>>>(ma, mb, sa, sb, M, N, K, vec_store, d, status);
+  const int64_t tiles = ((M + kGB - 1) / kGB) * ((N + kGBN - 1) / kGBN);
+  const unsigned grid = (unsigned)std::min<int64_t>(tiles, (int64_t)sm_count());
+  k<<<grid, kGThreads, kGSmemBytes, st>>>(ma, mb, md, sa, sb, M, N, K, d, status);
   return cudaGetLastError();
 }
 
-// The caller has checked: qa and qb 16-byte aligned, K a multiple of 16
-// (the tensor maps' row stride), M and N below 2^31 / 128 tiles.  Returns
+// The caller has checked: qa and qb 16-byte aligned, K a multiple of 128,
+// M, N, K below 2^31 and fewer than 2^30 tiles.  Returns
 // cudaErrorNotSupported when the tensor-map entry point is missing.
 cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
                                          const float* sb, int64_t M, int64_t N, int64_t K, int fmt,
@@ -552,15 +549,34 @@ cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, con
   if (!gemm_encode_fn()) return cudaErrorNotSupported;
   CUtensorMap ma, mb;
   if (encode_k_major(&ma, qa, M, K, kGB) != CUDA_SUCCESS ||
-      encode_k_major(&mb, qb, N, K, kGB) != CUDA_SUCCESS)
+      encode_k_major(&mb, qb, N, K, kGBN) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const int vec = (N % 8 == 0) && ((uintptr_t)d % 16 == 0);
-  if (fmt == GS_E4M3)
-    return out_dtype == GS_F32
-               ? gemm_t<GS_E4M3, GS_F32>(ma, mb, sa, sb, M, N, K, vec, d, status, st)
-               : gemm_t<GS_E4M3, GS_BF16>(ma, mb, sa, sb, M, N, K, vec, d, status, st);
-  return out_dtype == GS_F32 ? gemm_t<GS_E5M2, GS_F32>(ma, mb, sa, sb, M, N, K, vec, d, status, st)
-                             : gemm_t<GS_E5M2, GS_BF16>(ma, mb, sa, sb, M, N, K, vec, d, status, st);
+  // D through TMA stores when its base and row stride allow it (16 bytes).
+  CUtensorMap md;
+  memset(&md, 0, sizeof(md));
+  int tma_store = ((uintptr_t)d % 16 == 0) && (((size_t)N * esz) % 16 == 0);
+  if (tma_store) {
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)N * esz};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (gemm_encode_fn()(&md,
+                         out_dtype == GS_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, d, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const bool e4 = fmt == GS_E4M3, f32 = out_dtype == GS_F32;
+#define GS_GEMM_CALL(F, O, T) gemm_t<F, O, T>(ma, mb, md, sa, sb, M, N, K, d, status, st)
+  if (tma_store) {
+    if (e4) return f32 ? GS_GEMM_CALL(GS_E4M3, GS_F32, true) : GS_GEMM_CALL(GS_E4M3, GS_BF16, true);
+    return f32 ? GS_GEMM_CALL(GS_E5M2, GS_F32, true) : GS_GEMM_CALL(GS_E5M2, GS_BF16, true);
+  }
+  if (e4) return f32 ? GS_GEMM_CALL(GS_E4M3, GS_F32, false) : GS_GEMM_CALL(GS_E4M3, GS_BF16, false);
+  return f32 ? GS_GEMM_CALL(GS_E5M2, GS_F32, false) : GS_GEMM_CALL(GS_E5M2, GS_BF16, false);
+#undef GS_GEMM_CALL
 }
 
 }  // namespace gs

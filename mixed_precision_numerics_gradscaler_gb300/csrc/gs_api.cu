@@ -490,7 +490,7 @@ int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
   if (M < 0 || N < 0 || K < 0 || K % 128 != 0 || M >= (1LL << 31) || K >= (1LL << 31) ||
       N >= (1LL << 31) || !mul_ok(M, N) || !mul_ok(M * N, 4) || !mul_ok(M, K) || !mul_ok(N, K))
     return GS_ERR_SHAPE;
-  if (((M + 127) / 128) * ((N + 255) / 256) >= (1LL << 31)) return GS_ERR_SHAPE;  // tile count
+  if (((M + 127) / 128) * ((N + 255) / 256) >= (1LL << 30)) return GS_ERR_SHAPE;  // tile count
   if (M == 0 || N == 0) return GS_OK;
   if (!d || (K > 0 && (!qa || !sa || !qb || !sb))) return GS_ERR_NULL;
   const size_t dsz = out_dtype == GS_F32 ? 4 : 2, nd = (size_t)(M * N) * dsz;

@@ -120,6 +120,29 @@ def test_gemm_exact_values_bf16_output(gs, orc, fmt):
     _assert_exact(orc, got, want, BF16, f"bf16 fmt {fmt}")
 
 
+@pytest.mark.parametrize("M,N,K,out,offset", [
+    (260, 136, 256, BF16, 0),   # TMA stores, ragged tile columns (row stride 272 B)
+    (200, 130, 256, BF16, 0),   # row stride 260 B: element-wise stores
+    (150, 198, 384, F32, 0),    # row stride 792 B: element-wise stores
+    (300, 256, 256, F32, 1),    # D one element off 16-byte alignment: element-wise
+    (64, 72, 128, F32, 0),      # a single partial tile through TMA
+])
+def test_gemm_exact_values_store_paths(gs, orc, M, N, K, out, offset):
+    fmt = E4M3
+    qa, sa, qb, sb = _exact_inputs(orc, fmt, M, N, K, seed=M + 3 * N + K + offset)
+    want = orc.gemm_fp8_block(qa, sa, qb, sb, fmt)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    dt = torch.float32 if out == F32 else torch.bfloat16
+    buf = torch.full((M * N + offset,), float("nan"), dtype=dt, device=DEV)
+    d = buf[offset:].view(M, N)
+    gs.fp8_gemm_block_scaled(t(qa), t(sa), t(qb), t(sb), fmt, d)
+    torch.cuda.synchronize()
+    assert gs.gs_device_status() == 0
+    _assert_exact(orc, d, want, out, f"{M}x{N}x{K} out {out} offset {offset}")
+    if offset:
+        assert torch.isnan(buf[:offset]).all()  # nothing written before D
+
+
 def _tolerance(orc, qa, sa, qb, sb, fmt):
     absd = orc.gemm_fp8_block(qa & 0x7F, sa, qb & 0x7F, sb, fmt)
     nkb = qa.shape[1] // 128
