@@ -345,9 +345,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // swizzled layout (16-byte piece p of row r at p ^ (r % 8)) and stored
     // by one TMA instruction, which also clips rows and columns past D.
     uint8_t* const my_out = out_stage + (warp - 4) * kGOutBytes;
-    auto store_tile = [&](int64_t m, int64_t n0, bool live, const uint64_t (&acc)[kGB / 2]) {
+    // `between` runs once the first chunk is handed to TMA, overlapping the
+    // wait for its buffer (or before the element stores).
+    auto store_tile = [&](int64_t m, int64_t n0, bool live, const uint64_t (&acc)[kGB / 2],
+                          auto&& between) {
       if constexpr (TMA_STORE) {
-        if (!__any_sync(0xffffffffu, live)) return;
+        if (!__any_sync(0xffffffffu, live)) {
+          between();
+          return;
+        }
         constexpr int kCols = OUT == GS_F32 ? 32 : 64;  // columns per 128-byte chunk
 #pragma unroll
         for (int c = 0; c < kGB / kCols; ++c) {
@@ -375,8 +381,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
             g_tma_store(&map_d, my_out, (int32_t)(n0 + c * kCols), (int32_t)(m - lane));
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
+          if (c == 0) between();
         }
       } else {  // unaligned D or row stride: one element at a time
+        between();
         if (!live) return;
         const int64_t off = m * N + n0;
 #pragma unroll
@@ -394,30 +402,33 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
       }
     };
-    // This thread's row and column block of tile t, and its scale rows.
-    auto locate = [&](int t, int64_t& m, int64_t& n0, bool& live, const float*& sa_row,
-                      const float*& sb_row) {
-      int mt = 0, nt = 0;
+    // Tile t's raster coordinates (mt = -1 past the last tile), and from
+    // them this thread's row, column block and scale rows.
+    auto coords = [&](int t, int& mt, int& nt) {
+      mt = -1;
+      nt = 0;
       if (t < n_tiles) gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
+    };
+    auto derive = [&](int mt, int nt, int64_t& m, int64_t& n0, bool& live, const float*& sa_row,
+                      const float*& sb_row) {
       m = (int64_t)mt * kGB + row;
       n0 = (int64_t)nt * kGBN + h * kGB;
-      live = t < n_tiles && m < M && n0 < N;  // rows / columns past the edge were zeros
+      live = mt >= 0 && m < M && n0 < N;  // rows / columns past the edge were zeros
       sa_row = sa + (live ? m * nkb : 0);
       sb_row = sb + (live ? (n0 / kGB) * nkb : 0);
     };
+    int mt, nt, mt_n, nt_n;  // this tile and the next
+    coords(blockIdx.x, mt, nt);
+    coords(blockIdx.x + gridDim.x, mt_n, nt_n);
     int64_t m, n0;
     bool live;
     const float *sa_row, *sb_row;
-    locate(blockIdx.x, m, n0, live, sa_row, sb_row);
+    derive(mt, nt, m, n0, live, sa_row, sb_row);
     float sa_v = live ? sa_row[0] : 0.0f, sb_v = live ? sb_row[0] : 0.0f;
     const int kb_ahead = nkb > 4 ? nkb - 4 : 0;  // when to fetch the next tile's first scales
     uint32_t it = 0;
     bool go = true;
     for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
-      int64_t m_n, n0_n;
-      bool live_n;
-      const float *sa_row_n, *sb_row_n;
-      locate(t + gridDim.x, m_n, n0_n, live_n, sa_row_n, sb_row_n);
       float sa_first_n = 0.0f, sb_first_n = 0.0f;
       uint64_t acc[kGB / 2];  // column pairs (2j, 2j + 1)
 #pragma unroll
@@ -430,9 +441,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
           sa_v = sa_row[kb + 1];
           sb_v = sb_row[kb + 1];
         }
-        if (kb == kb_ahead && live_n) {  // the next tile's, well ahead of its start
-          sa_first_n = sa_row_n[0];
-          sb_first_n = sb_row_n[0];
+        if (kb == kb_ahead) {  // the next tile's, well ahead of its start
+          int64_t m_x, n0_x;
+          bool live_x;
+          const float *sa_x, *sb_x;
+          derive(mt_n, nt_n, m_x, n0_x, live_x, sa_x, sb_x);
+          if (live_x) {
+            sa_first_n = sa_x[0];
+            sb_first_n = sb_x[0];
+          }
         }
         // the warp leaves together: tcgen05.ld below needs all 32 lanes
         const bool got = g_wait(&tfull[b], (it >> 1) & 1u, abort_flag, status);
@@ -465,12 +482,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
       }
       if (!go || *abort_flag) break;
-      store_tile(m, n0, live, acc);
-      m = m_n;
-      n0 = n0_n;
-      live = live_n;
-      sa_row = sa_row_n;
-      sb_row = sb_row_n;
+      int mt_2, nt_2;  // the tile after next, located while TMA drains
+      store_tile(m, n0, live, acc, [&] { coords(t + 2 * (int)gridDim.x, mt_2, nt_2); });
+      derive(mt_n, nt_n, m, n0, live, sa_row, sb_row);
+      mt_n = mt_2;
+      nt_n = nt_2;
       sa_v = sa_first_n;
       sb_v = sb_first_n;
     }
