@@ -61,7 +61,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--only", choices=["unscale", "quant_1x128", "dequant", "quant_128x128",
                                       "quant_tensor", "quant_mx", "dequant_mx", "quant_delayed",
-                                      "unscale_norm", "master_update"],
+                                      "unscale_norm", "master_update", "gemm"],
                    help="time one kernel alone on a small case (for ncu captures)")
     return p.parse_args(argv)
 
@@ -97,6 +97,20 @@ def throughput(total_bytes: float, elapsed_s: float) -> float:
 
 
 # ---- peaks, traffic, clocks --------------------------------------------------------
+
+def fp8_peak(timed_s: float) -> tuple[float, str]:
+    """Dense FP8 tensor peak: a measured bf16 GEMM rate x 2 (the nominal
+    FP8 / bf16 ratio of the part) -- the sustained (power-capped) rate when
+    the timed loop runs for half a second or more, else the burst rate."""
+    sustained = timed_s >= 0.5
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        return 2.0 * float(pk[key]), f"measured {key} x 2"
+    except Exception:
+        return 2.0 * (1700.0 if sustained else 1900.0), "fallback bf16 x 2"
+
 
 def hbm_peak() -> tuple[float, str]:
     try:
@@ -662,6 +676,26 @@ def run_only(args):
         else:
             fn = lambda: gs.fp8_dequant_mx(q, s, "e4m3", y)
         nbytes = 3 * a.numel + a.numel // 32
+    elif args.only == "gemm":
+        # the consumer: activations [16384 tokens, 8192] (1x128 E4M3 tiles)
+        # times a weight [28672, 8192] (128x128 E4M3 tiles), bf16 out
+        a = wl.cfg3_act()
+        w = wl.cfg4_weight(rows=28672, cols=8192)
+        x = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
+        dg.fill_device(a.spec, 0, a.numel, x.data_ptr(), st)
+        wt = torch.empty(w.rows, w.cols, dtype=torch.bfloat16, device=dev)
+        dg.fill_device(w.spec, 0, w.numel, wt.data_ptr(), st)
+        qa = torch.empty(a.rows, a.cols, dtype=torch.uint8, device=dev)
+        sa = torch.empty(a.rows, a.cols // 128, dtype=torch.float32, device=dev)
+        qb = torch.empty(w.rows, w.cols, dtype=torch.uint8, device=dev)
+        sb = torch.empty(w.rows // 128, w.cols // 128, dtype=torch.float32, device=dev)
+        gs.fp8_quant_block(x, 1, 128, "e4m3", qa, sa)
+        gs.fp8_quant_block(wt, 128, 128, "e4m3", qb, sb)
+        del x, wt
+        d = torch.empty(a.rows, w.rows, dtype=torch.bfloat16, device=dev)
+        fn = lambda: gs.fp8_gemm_block_scaled(qa, sa, qb, sb, "e4m3", d)
+        flops = 2 * a.rows * w.rows * a.cols
+        nbytes = None
     elif args.only == "quant_128x128":
         w = wl.cfg4_weight()
         x = torch.empty(w.rows, w.cols, dtype=torch.bfloat16, device=dev)
@@ -697,20 +731,30 @@ def run_only(args):
     # does not land inside the interval (inputs exceed L2: no flush needed)
     reps = 10
     ts = []
-    for _ in range(args.steps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        fn()
-        e0.record()
-        for _ in range(reps):
+    with ClockSampler(gpu_uuid(torch, 0)) as clocks:
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             fn()
-        e1.record()
-        torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1) / reps)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps)
     ms = statistics.median(ts)
+    clk = clocks.summary()
+    if nbytes is None:  # tensor-bound: FLOP/s against the FP8 peak
+        peak, src = fp8_peak(sum(ts) * reps / 1e3)
+        tf = flops / ms / 1e9
+        print(json.dumps({"only": args.only, "flops": flops, "median_ms": ms, "tflops": tf,
+                          "frac": tf / peak, "peak_tflops": peak, "peak_source": src,
+                          "gpu_status": gs.gs_device_status(), "clocks": clk,
+                          "steps": args.steps}), flush=True)
+        return 0
     peak, src = hbm_peak()
     print(json.dumps({"only": args.only, "bytes": nbytes, "median_ms": ms, "gbs": nbytes / ms / 1e6,
                       "frac": nbytes / ms / 1e6 / peak, "peak": peak, "peak_source": src,
-                      "steps": args.steps}), flush=True)
+                      "clocks": clk, "steps": args.steps}), flush=True)
     return 0
 
 
