@@ -73,6 +73,7 @@ def _load_lib() -> ctypes.CDLL:
         "gs_unscale_check_update_noalloc": (ci, [vp, vp, vp, i32, vp, vp, vp, vp, f32, f32, i32, vp]),
         "gs_noalloc_limits": (ci, [ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64)]),
         "fp8_gemm_block_scaled": (ci, [vp, vp, vp, vp, i64, i64, i64, ci, ci, vp, vp]),
+        "gs_test_set_stall": (ci, [ci]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -364,6 +365,12 @@ def fp8_gemm_block_scaled(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, 
     _check(_lib.fp8_gemm_block_scaled(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _FMTS[fmt],
                                       _DTYPES[d.dtype], _ptr(d), _stream(stream)),
            "fp8_gemm_block_scaled")
+
+
+def gs_test_set_stall(on: bool) -> None:
+    """Test hook: the TMA-fed kernels issue no loads while on, so their
+    bounded waits run out and they report GS_ERR_TIMEOUT."""
+    _check(_lib.gs_test_set_stall(1 if on else 0), "gs_test_set_stall")
 
 
 def gs_device_status(stream=None) -> int:

@@ -28,7 +28,7 @@ def _sources():
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "gsfp8.h"), __file__]
+        glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
 def up_to_date() -> bool:

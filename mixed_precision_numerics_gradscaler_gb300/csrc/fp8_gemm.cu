@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                           const __grid_constant__ CUtensorMap map_b,
                           const __grid_constant__ CUtensorMap map_d, const float* __restrict__ sa,
                           const float* __restrict__ sb, int64_t M, int64_t N, int64_t K,
-                          void* __restrict__ d, int32_t* status) {
+                          void* __restrict__ d, int32_t* status, int stall) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the swizzled tiles
   const uint32_t pad = (1024u - (g_smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGCtrlRegs));
     if (warp == 0 && lane == 0) {  // TMA producer
       uint32_t it = 0;  // K-blocks issued so far over this CTA's tiles (mod 2^32)
-      bool go = true;
+      bool go = !stall;  // stall: test hook, no loads, so the MMA's wait runs out
       for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
         int mt, nt;
         gemm_tile_coords(t, tiles_m, tiles_n, mt, nt);
@@ -548,7 +548,7 @@ static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = ((M + kGB - 1) / kGB) * ((N + kGBN - 1) / kGBN);
   const unsigned grid = (unsigned)std::min<int64_t>(tiles, (int64_t)sm_count());
-  k<<<grid, kGThreads, kGSmemBytes, st>>>(ma, mb, md, sa, sb, M, N, K, d, status);
+  k<<<grid, kGThreads, kGSmemBytes, st>>>(ma, mb, md, sa, sb, M, N, K, d, status, test_stall());
   return cudaGetLastError();
 }
 

@@ -81,7 +81,7 @@ template <typename Tag, int FMT>
 __global__ void __launch_bounds__(kTmaThreads)
     quant_128x128_tma(const __grid_constant__ CUtensorMap map, int64_t nbr, int64_t nbc,
                       uint8_t* __restrict__ q, int64_t C, float* __restrict__ scales,
-                      int32_t* status) {
+                      int32_t* status, int stall) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kTileBytes);
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kTmaThreads)
                   (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * 128));
   };
   int64_t issued = 0;
-  if (tid == 0)
+  if (tid == 0 && !stall)  // stall: test hook, no loads, so the first wait runs out
     for (; issued < kTmaStages && issued < my_n; ++issued) issue(issued);
 
   // Thread tid owns rows (tid >> 4) + kRowsPerPass * j, 16-byte column chunk
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kTmaThreads)
     uint32_t* rb = red + (k & 1) * kTmaWarps;
     if (lane == 0) rb[warp] = m;
     __syncthreads();  // every thread holds its part of the tile: the stage is free
-    if (tid == 0 && issued < my_n) issue(issued++);
+    if (tid == 0 && issued < my_n && !stall) issue(issued++);
     m = 0;
 #pragma unroll
     for (int w = 0; w < kTmaWarps; ++w) m = max(m, rb[w]);
@@ -191,7 +191,8 @@ static cudaError_t launch_tma_t(const CUtensorMap& map, int64_t R, int64_t C, ui
   const int64_t nbr = R / 128, nbc = C / 128;
   int64_t grid = (int64_t)sm_count() * occ;
   if (grid > nbr * nbc) grid = nbr * nbc;
-  k<<<(unsigned)grid, kTmaThreads, kTmaSmemBytes, st>>>(map, nbr, nbc, q, C, scales, status);
+  k<<<(unsigned)grid, kTmaThreads, kTmaSmemBytes, st>>>(map, nbr, nbc, q, C, scales, status,
+                                                        test_stall());
   return cudaGetLastError();
 }
 

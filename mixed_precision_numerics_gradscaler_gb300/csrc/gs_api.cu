@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <new>
@@ -12,6 +13,7 @@
 
 #include "gs_internal.h"
 #include "gsfp8.h"
+#include "gsfp8_test.h"
 
 // The device status word (GS_OK or GS_ERR_TIMEOUT), one per device.
 __device__ int32_t g_gs_device_status = 0;
@@ -108,6 +110,9 @@ static bool valid_dtype(int dt) { return dt == GS_F16 || dt == GS_BF16 || dt == 
 static bool valid_fmt(int f) { return f == GS_E4M3 || f == GS_E5M2; }
 
 static bool mul_ok(int64_t a, int64_t b) { return a >= 0 && b >= 0 && (b == 0 || a <= INT64_MAX / b); }
+
+static std::atomic<int> g_test_stall{0};
+int test_stall() { return g_test_stall.load(std::memory_order_relaxed); }
 
 }  // namespace gs
 
@@ -514,6 +519,11 @@ int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
   cudaError_t e = launch_gemm_fp8_block_scaled(qa, sa, qb, sb, M, N, K, fmt, out_dtype, d, status,
                                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
+}
+
+int gs_test_set_stall(int on) {
+  g_test_stall.store(on ? 1 : 0, std::memory_order_relaxed);
+  return GS_OK;
 }
 
 int gs_device_status(int32_t* h_status, void* stream) {

@@ -57,6 +57,10 @@ int current_device();
 // Records e as the calling thread's last CUDA error (gs_last_cuda_error).
 void record_cuda_error(cudaError_t e);
 
+// Test hook (gs_test_set_stall): nonzero makes the TMA-fed kernels issue no
+// loads, so that their bounded waits run out.
+int test_stall();
+
 // Launchers.  Each returns the launch's cudaError_t.
 cudaError_t launch_unscale_check_update(const Chunk* d_chunks, int64_t n_chunks, ListWs* ws,
                                         float* scale, int32_t* tracker, int32_t* found,

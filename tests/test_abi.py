@@ -1,6 +1,7 @@
-"""The C ABI library loads, exports every entry point include/gsfp8.h
-declares, and rejects bad arguments on the host before touching CUDA."""
+"""The C ABI library loads, exports every entry point include/*.h declares,
+and rejects bad arguments on the host before touching CUDA."""
 import ctypes
+import glob
 import os
 import re
 
@@ -8,13 +9,15 @@ import pytest
 
 from conftest import ROOT
 
-HEADER = os.path.join(ROOT, "include", "gsfp8.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def _declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", src, flags=re.M)))
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -27,7 +30,8 @@ def test_header_declares_the_path(gs):
     names = _declared_functions()
     for fn in ["gs_unscale_check_update", "fp8_quant_block", "fp8_quant_tensor", "fp8_dequant",
                "gs_tensor_list_create", "gs_tensor_list_destroy", "gs_scaler_state_get",
-               "gs_scaler_state_set", "gs_status_str", "gs_ws_bytes", "gs_device_status"]:
+               "gs_scaler_state_set", "gs_status_str", "gs_ws_bytes", "gs_device_status",
+               "fp8_gemm_block_scaled", "gs_test_set_stall"]:
         assert fn in names
 
 
