@@ -153,6 +153,34 @@ def test_fp8_encoder_matches_library_cast_after_clamp(orc, fmt, tdt):
     assert orc.fp8_encode(-float("nan"), fmt) == 0x7F
 
 
+@pytest.mark.parametrize("fmt,tdt", [(E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)])
+def test_fp8_encoder_exhaustive_over_every_fp32_pattern(orc, fmt, tdt):
+    """All 2^32 fp32 bit patterns: every non-NaN input encodes as torch's
+    cast after clamping to +-MAX (an independent RNE implementation), every
+    NaN pattern (either sign, any payload) to 0x7F. Chunks of 2^24 patterns
+    run on the host threads (the oracle is C behind ctypes, which releases
+    the GIL)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    mx = orc.fp8_max(fmt)
+    chunk = 1 << 24
+
+    def check(k):
+        bits = np.arange(k * chunk, (k + 1) * chunk, dtype=np.uint64).astype(np.uint32)
+        x = bits.view(np.float32)
+        got = orc.fp8_encode_array(x, fmt)
+        nan = np.isnan(x)
+        lib = torch.from_numpy(np.where(nan, np.float32(0), x)).clamp(-mx, mx).to(tdt)
+        want = np.where(nan, np.uint8(0x7F), lib.view(torch.uint8).numpy())
+        bad = np.nonzero(got != want)[0]
+        return [(hex(int(bits[i])), hex(got[i]), hex(want[i])) for i in bad[:3]]
+
+    workers = max(1, min(16, len(os.sched_getaffinity(0))))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        bad = [b for r in ex.map(check, range((1 << 32) // chunk)) for b in r]
+    assert not bad, bad[:5]
+
+
 # ---- FP16 / BF16 ------------------------------------------------------------
 
 def test_f16_encoder_matches_numpy_float16(orc):

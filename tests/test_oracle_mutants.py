@@ -112,8 +112,10 @@ PINS_FOR = {
 
 def _run_pins(lib, pins):
     env = dict(os.environ, GS_ORACLE_LIB=lib)
+    # the exhaustive 2^32 encoder sweep runs once in the main suite, not per mistake
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "-m", "not gpu", *pins], cwd=ROOT, env=env, capture_output=True, text=True)
+                        "-m", "not gpu", "-k", "not exhaustive_over_every", *pins], cwd=ROOT,
+                       env=env, capture_output=True, text=True)
     return r.returncode
 
 
