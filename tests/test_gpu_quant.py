@@ -323,3 +323,46 @@ def test_quant_deterministic(gs):
         outs.append((q.cpu().numpy(), s.cpu().numpy()))
     for o in outs[1:]:
         assert (o[0] == outs[0][0]).all() and (o[1] == outs[0][1]).all()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_exhaustive_fp32_cast_at_unit_scale(gs, orc, fmt):
+    """Every fp32 value with |x| <= MAX (about 2.3e9 bit patterns per
+    format, both signs): per-tensor quantisation of a chunk that also holds
+    MAX itself has amax = MAX, so s = MAX / MAX = 1 exactly and the codes
+    are the device's FP8 encoding of x. Compared element by element with the
+    oracle's encoder (itself pinned on all 2^32 patterns), run on the host
+    threads."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    F = orc.E4M3 if fmt == "e4m3" else orc.E5M2
+    mx = orc.fp8_max(F)
+    top = int(np.array([mx], np.float32).view(np.uint32)[0])     # bit pattern of +MAX
+    chunk = 1 << 27
+    ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=DEV)
+    q = torch.empty(chunk + 1, dtype=torch.uint8, device=DEV)
+    s = torch.empty(1, dtype=torch.float32, device=DEV)
+    workers = max(1, min(16, len(os.sched_getaffinity(0))))
+    pieces = 4 * workers
+
+    def oracle_codes(bits):
+        x = bits.view(np.float32)
+        step = (x.size + pieces - 1) // pieces
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            parts = ex.map(lambda i: orc.fp8_encode_array(x[i:i + step], F), range(0, x.size, step))
+        return np.concatenate(list(parts))
+
+    for base in (0, -(1 << 31)):                 # +x patterns, then the sign-bit-set ones
+        for start in range(0, top + 1, chunk):
+            n = min(chunk, top + 1 - start)
+            bits_d = torch.arange(base + start, base + start + n, dtype=torch.int32, device=DEV)
+            x = torch.cat([bits_d.view(torch.float32), torch.tensor([mx], dtype=torch.float32,
+                                                                    device=DEV)])
+            gs.fp8_quant_tensor(x, fmt, q[:n + 1], s, ws)
+            got = q[:n].cpu().numpy()
+            assert float(s.item()) == 1.0
+            bits = (np.arange(start, start + n, dtype=np.uint64) +
+                    np.uint64(0 if base == 0 else 1 << 31)).astype(np.uint32)
+            want = oracle_codes(bits)
+            bad = np.nonzero(got != want)[0]
+            assert bad.size == 0, [(hex(int(bits[i])), hex(got[i]), hex(want[i])) for i in bad[:5]]
