@@ -34,7 +34,10 @@ constexpr int kRowPasses = 128 / kRowsPerPass;
 constexpr int kTmaStages = 3;
 constexpr int kTileBytes = 128 * 128 * 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kTmaSmemBytes = kTmaStages * kTileBytes + kTmaStages * 8 + 2 * kTmaWarps * 4 + 64;
+// tiles, then the stage barriers, then (16-byte aligned) two rows of
+// per-warp maxima
+constexpr int kRedOffset = (kTmaStages * kTileBytes + kTmaStages * 8 + 15) / 16 * 16;
+constexpr int kTmaSmemBytes = kRedOffset + 2 * kTmaWarps * 4 + 64;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kTmaThreads)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kTileBytes);
-  uint32_t* red = reinterpret_cast<uint32_t*>(full + kTmaStages);  // [2][kTmaWarps]
+  uint32_t* red = reinterpret_cast<uint32_t*>(smem + kRedOffset);  // [2][kTmaWarps]
 
   const int64_t n_blocks = nbr * nbc;
   if ((int64_t)blockIdx.x >= n_blocks) return;
@@ -97,21 +100,38 @@ __global__ void __launch_bounds__(kTmaThreads)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  auto issue = [&](int64_t k) {
-    const int64_t b = blockIdx.x + k * gridDim.x;
-    tma_load_tile(&map, &full[k % kTmaStages], tiles + (k % kTmaStages) * kTileBytes,
-                  (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * 128));
+  // Block b = blockIdx.x + k * gridDim.x is (row b / nbc, column b % nbc);
+  // walking k, both advance by gridDim.x's quotient and remainder, so no
+  // division is left in the loop.
+  const int64_t step_r = gridDim.x / nbc, step_c = gridDim.x % nbc;
+  auto advance = [&](int64_t& br, int64_t& bc) {
+    br += step_r;
+    bc += step_c;
+    if (bc >= nbc) {
+      bc -= nbc;
+      ++br;
+    }
   };
+  int64_t ibr = blockIdx.x / nbc, ibc = blockIdx.x % nbc;  // next block to load
+  uint32_t istage = 0;
   int64_t issued = 0;
+  auto issue = [&]() {
+    tma_load_tile(&map, &full[istage], tiles + istage * kTileBytes, (int32_t)(ibc * 128),
+                  (int32_t)(ibr * 128));
+    advance(ibr, ibc);
+    istage = istage + 1 == kTmaStages ? 0 : istage + 1;
+    ++issued;
+  };
   if (tid == 0 && !stall)  // stall: test hook, no loads, so the first wait runs out
-    for (; issued < kTmaStages && issued < my_n; ++issued) issue(issued);
+    while (issued < kTmaStages && issued < my_n) issue();
 
   // Thread tid owns rows (tid >> 4) + kRowsPerPass * j, 16-byte column chunk
   // (tid & 15): a warp reads two whole 256-byte rows per pass.
   const int row0 = tid >> 4, chunk = tid & 15;
+  int64_t br = blockIdx.x / nbc, bc = blockIdx.x % nbc;  // this block
+  uint32_t stage = 0, phase = 0;
   for (int64_t k = 0; k < my_n; ++k) {
-    const int stage = (int)(k % kTmaStages);
-    const bool ok = mbar_wait_bounded(&full[stage], (uint32_t)((k / kTmaStages) & 1));
+    const bool ok = mbar_wait_bounded(&full[stage], phase);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         atomicExch(status, (int32_t)GS_ERR_TIMEOUT);
@@ -137,16 +157,22 @@ __global__ void __launch_bounds__(kTmaThreads)
     uint32_t* rb = red + (k & 1) * kTmaWarps;
     if (lane == 0) rb[warp] = m;
     __syncthreads();  // every thread holds its part of the tile: the stage is free
-    if (tid == 0 && issued < my_n && !stall) issue(issued++);
-    m = 0;
+    if (tid == 0 && issued < my_n && !stall) issue();
+    {
+      const uint4* r4 = reinterpret_cast<const uint4*>(rb);
+      uint4 a = r4[0];
 #pragma unroll
-    for (int w = 0; w < kTmaWarps; ++w) m = max(m, rb[w]);
+      for (int w = 1; w < kTmaWarps / 4; ++w) {
+        const uint4 c = r4[w];
+        a = make_uint4(max(a.x, c.x), max(a.y, c.y), max(a.z, c.z), max(a.w, c.w));
+      }
+      m = max(max(a.x, a.y), max(a.z, a.w));
+    }
     const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
     const bool fin = isfinite(s);
     const float r = __frcp_rn(s);
-    const int64_t b = blockIdx.x + k * gridDim.x;
-    const int64_t r0 = (b / nbc) * 128, c0 = (b % nbc) * 128;
-    if (tid == 0) scales[b] = s;
+    const int64_t r0 = br * 128, c0 = bc * 128;
+    if (tid == 0) scales[br * nbc + bc] = s;
 #pragma unroll
     for (int j = 0; j < kRowPasses; ++j) {
       uint2 o;
@@ -155,6 +181,11 @@ __global__ void __launch_bounds__(kTmaThreads)
       o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].z), lo16<Tag>(v[j].z), s, r, fin) |
             (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].w), lo16<Tag>(v[j].w), s, r, fin) << 16);
       st_stream(reinterpret_cast<uint2*>(q + (r0 + row0 + kRowsPerPass * j) * C + c0 + chunk * 8), o);
+    }
+    advance(br, bc);
+    if (++stage == kTmaStages) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
 }
