@@ -534,18 +534,21 @@ static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const CU
                           const float* sa, const float* sb, int64_t M, int64_t N, int64_t K,
                           void* d, int32_t* status, cudaStream_t st) {
   auto k = gemm_fp8_block_scaled<FMT, OUT, TMA_STORE>;
+  // The setmaxnreg split is sized for exactly kGLaunchRegs per thread at
+  // launch; a build that allocated another count must not run.
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
+  static cudaError_t regs_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
-    // The setmaxnreg split is sized for exactly kGLaunchRegs per thread at
-    // launch; a build that allocated another count must not run.
     cudaFuncAttributes fa;
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, k);
-    if (attr_err == cudaSuccess && fa.numRegs != kGLaunchRegs)
-      attr_err = cudaErrorInvalidConfiguration;
+    regs_err = cudaFuncGetAttributes(&fa, k);
+    if (regs_err == cudaSuccess && fa.numRegs != kGLaunchRegs)
+      regs_err = cudaErrorInvalidConfiguration;
   });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (regs_err != cudaSuccess) return regs_err;
+  int occ = 0;  // also raises the shared-memory limit on this device
+  const cudaError_t e = kernel_blocks_per_sm((const void*)k, kGThreads, kGSmemBytes, &occ);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
   const int64_t tiles = ((M + kGB - 1) / kGB) * ((N + kGBN - 1) / kGBN);
   const unsigned grid = (unsigned)std::min<int64_t>(tiles, (int64_t)sm_count());
   k<<<grid, kGThreads, kGSmemBytes, st>>>(ma, mb, md, sa, sb, M, N, K, d, status, test_stall());

@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 template <typename K>
 static int64_t persistent_grid(K kernel, int64_t work_items_per_cta_slot, int64_t n_items) {
   int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kQuantThreads, 0);
+  if (kernel_blocks_per_sm((const void*)kernel, kQuantThreads, 0, &occ) != cudaSuccess) occ = 1;
   if (occ < 1) occ = 1;
   int64_t grid = (int64_t)sm_count() * occ;
   const int64_t need = (n_items + work_items_per_cta_slot - 1) / work_items_per_cta_slot;

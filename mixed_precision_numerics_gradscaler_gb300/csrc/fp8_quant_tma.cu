@@ -211,14 +211,10 @@ template <typename Tag, int FMT>
 static cudaError_t launch_tma_t(const CUtensorMap& map, int64_t R, int64_t C, uint8_t* q,
                                 float* scales, int32_t* status, cudaStream_t st) {
   auto k = quant_128x128_tma<Tag, FMT>;
-  static int occ = 0;
-  if (occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kTmaThreads, kTmaSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-  }
+  int occ = 0;
+  const cudaError_t e = kernel_blocks_per_sm((const void*)k, kTmaThreads, kTmaSmemBytes, &occ);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
   const int64_t nbr = R / 128, nbc = C / 128;
   int64_t grid = (int64_t)sm_count() * occ;
   if (grid > nbr * nbc) grid = nbr * nbc;

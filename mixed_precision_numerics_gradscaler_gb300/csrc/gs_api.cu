@@ -7,8 +7,10 @@
 
 #include <atomic>
 #include <cmath>
+#include <map>
 #include <mutex>
 #include <new>
+#include <tuple>
 #include <vector>
 
 #include "gs_internal.h"
@@ -46,15 +48,37 @@ int current_device() {
 }
 
 int sm_count() {
-  static int cache[kMaxDevices] = {0};
+  static std::atomic<int> cache[kMaxDevices] = {};
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return 1;
-  if (cache[d] == 0) {
-    int n = 0;
+  int n = cache[d].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
-    cache[d] = n > 0 ? n : 1;
+    if (n < 1) n = 1;
+    cache[d].store(n, std::memory_order_relaxed);
   }
-  return cache[d];
+  return n;
+}
+
+cudaError_t kernel_blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* blocks) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int>, int> cache;
+  const auto key = std::make_tuple(kernel, current_device(), threads, smem_bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    if (smem_bytes > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           smem_bytes);
+      if (e != cudaSuccess) return e;
+    }
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem_bytes);
+    if (e != cudaSuccess) return e;
+    it = cache.emplace(key, occ).first;
+  }
+  *blocks = it->second;
+  return cudaSuccess;
 }
 
 void record_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }

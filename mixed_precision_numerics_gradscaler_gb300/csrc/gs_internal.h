@@ -52,6 +52,12 @@ struct ScalerPolicy {
 
 // Cached device properties of the current device.
 int sm_count();
+
+// Resident blocks per SM of `kernel` at (threads, dynamic smem bytes) on the
+// current device; the first call per kernel and device also raises the
+// kernel's dynamic shared-memory limit there (function attributes are per
+// device).  Thread-safe; cached.
+cudaError_t kernel_blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* blocks);
 int current_device();
 
 // Records e as the calling thread's last CUDA error (gs_last_cuda_error).
