@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <map>
@@ -135,6 +136,25 @@ static bool valid_fmt(int f) { return f == GS_E4M3 || f == GS_E5M2; }
 
 static bool mul_ok(int64_t a, int64_t b) { return a >= 0 && b >= 0 && (b == 0 || a <= INT64_MAX / b); }
 
+bool spans_conflict(Span* writes, size_t n_writes, const Span* reads, size_t n_reads) {
+  size_t k = 0;  // drop empty ranges
+  for (size_t i = 0; i < n_writes; ++i)
+    if (writes[i].hi > writes[i].lo) writes[k++] = writes[i];
+  std::sort(writes, writes + k, [](const Span& a, const Span& b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < k; ++i)
+    if (writes[i].lo < writes[i - 1].hi) return true;
+  // the written ranges are now disjoint and sorted by both ends: a read range
+  // meets one only if it meets the last one starting before its end
+  for (size_t i = 0; i < n_reads; ++i) {
+    const Span r = reads[i];
+    if (r.hi <= r.lo) continue;
+    const Span* w = std::lower_bound(writes, writes + k, r.hi,
+                                     [](const Span& a, uintptr_t v) { return a.lo < v; });
+    if (w != writes && (w - 1)->hi > r.lo) return true;
+  }
+  return false;
+}
+
 static std::atomic<int> g_test_stall{0};
 int test_stall() { return g_test_stall.load(std::memory_order_relaxed); }
 
@@ -169,19 +189,29 @@ int gs_tensor_list_create(const void* const* grads, void* const* outs, const int
   if (n_tensors > 0 && (!grads || !outs || !numels)) return GS_ERR_NULL;
   std::vector<Chunk> chunks;
   int64_t total = 0;
-  for (int32_t i = 0; i < n_tensors; ++i) {
-    const int64_t n = numels[i];
-    if (n < 0 || n > (INT64_MAX >> 3)) return GS_ERR_SHAPE;
-    if (n == 0) continue;
-    if (!grads[i] || !outs[i]) return GS_ERR_NULL;
-    if (!aligned(grads[i], 2) || !aligned(outs[i], 4)) return GS_ERR_ARG;
-    if (!device_reachable(grads[i]) || !device_reachable(outs[i])) return GS_ERR_ARG;
-    if (overlaps(grads[i], (size_t)n * 2, outs[i], (size_t)n * 4)) return GS_ERR_ARG;
-    const uint16_t* g = static_cast<const uint16_t*>(grads[i]);
-    float* o = static_cast<float*>(outs[i]);
-    for (int64_t off = 0; off < n; off += kChunkElems)
-      chunks.push_back(Chunk{g + off, o + off, (n - off) < kChunkElems ? (n - off) : kChunkElems});
-    total += n;
+  try {  // nothing may throw across the C ABI (a vector that cannot grow)
+    std::vector<Span> written, read;
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      const int64_t n = numels[i];
+      if (n < 0 || n > (INT64_MAX >> 3) || total > INT64_MAX - n) return GS_ERR_SHAPE;
+      if (n == 0) continue;
+      if (!grads[i] || !outs[i]) return GS_ERR_NULL;
+      if (!aligned(grads[i], 2) || !aligned(outs[i], 4)) return GS_ERR_ARG;
+      if (!device_reachable(grads[i]) || !device_reachable(outs[i])) return GS_ERR_ARG;
+      written.push_back(Span{(uintptr_t)outs[i], (uintptr_t)outs[i] + (uintptr_t)n * 4});
+      read.push_back(Span{(uintptr_t)grads[i], (uintptr_t)grads[i] + (uintptr_t)n * 2});
+      const uint16_t* g = static_cast<const uint16_t*>(grads[i]);
+      float* o = static_cast<float*>(outs[i]);
+      for (int64_t off = 0; off < n; off += kChunkElems)
+        chunks.push_back(Chunk{g + off, o + off, (n - off) < kChunkElems ? (n - off) : kChunkElems});
+      total += n;
+    }
+    // one launch covers every tensor: no output may overlap any input or
+    // any other output
+    if (spans_conflict(written.data(), written.size(), read.data(), read.size()))
+      return GS_ERR_ARG;
+  } catch (...) {
+    return GS_ERR_ARG;
   }
   gs_tensor_list* l =
       new (std::nothrow) gs_tensor_list{current_device(), nullptr, 0, total, nullptr, nullptr};
@@ -280,23 +310,33 @@ int gs_param_list_create(float* const* master, uint16_t* const* master_bf16,
   if (n_tensors > 0 && (!master || !grads || !numels)) return GS_ERR_NULL;
   std::vector<MChunk> chunks;
   int64_t total = 0;
-  for (int32_t i = 0; i < n_tensors; ++i) {
-    const int64_t n = numels[i];
-    if (n < 0 || n > (INT64_MAX >> 3)) return GS_ERR_SHAPE;
-    if (n == 0) continue;
-    uint16_t* wb = master_bf16 ? master_bf16[i] : nullptr;
-    if (!master[i] || !grads[i]) return GS_ERR_NULL;
-    if (!aligned(master[i], 4) || !aligned(grads[i], 4) || (wb && !aligned(wb, 2))) return GS_ERR_ARG;
-    if (!device_reachable(master[i]) || !device_reachable(grads[i]) || (wb && !device_reachable(wb)))
+  try {  // nothing may throw across the C ABI (a vector that cannot grow)
+    std::vector<Span> written, read;
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      const int64_t n = numels[i];
+      if (n < 0 || n > (INT64_MAX >> 3) || total > INT64_MAX - n) return GS_ERR_SHAPE;
+      if (n == 0) continue;
+      uint16_t* wb = master_bf16 ? master_bf16[i] : nullptr;
+      if (!master[i] || !grads[i]) return GS_ERR_NULL;
+      if (!aligned(master[i], 4) || !aligned(grads[i], 4) || (wb && !aligned(wb, 2)))
+        return GS_ERR_ARG;
+      if (!device_reachable(master[i]) || !device_reachable(grads[i]) ||
+          (wb && !device_reachable(wb)))
+        return GS_ERR_ARG;
+      written.push_back(Span{(uintptr_t)master[i], (uintptr_t)master[i] + (uintptr_t)n * 4});
+      if (wb) written.push_back(Span{(uintptr_t)wb, (uintptr_t)wb + (uintptr_t)n * 2});
+      read.push_back(Span{(uintptr_t)grads[i], (uintptr_t)grads[i] + (uintptr_t)n * 4});
+      for (int64_t off = 0; off < n; off += kChunkElems)
+        chunks.push_back(MChunk{master[i] + off, wb ? wb + off : nullptr, grads[i] + off,
+                                (n - off) < kChunkElems ? (n - off) : kChunkElems});
+      total += n;
+    }
+    // masters and bf16 copies are written: none may overlap another one or a
+    // gradient
+    if (spans_conflict(written.data(), written.size(), read.data(), read.size()))
       return GS_ERR_ARG;
-    if (overlaps(master[i], (size_t)n * 4, grads[i], (size_t)n * 4) ||
-        (wb && (overlaps(wb, (size_t)n * 2, master[i], (size_t)n * 4) ||
-                overlaps(wb, (size_t)n * 2, grads[i], (size_t)n * 4))))
-      return GS_ERR_ARG;
-    for (int64_t off = 0; off < n; off += kChunkElems)
-      chunks.push_back(MChunk{master[i] + off, wb ? wb + off : nullptr, grads[i] + off,
-                              (n - off) < kChunkElems ? (n - off) : kChunkElems});
-    total += n;
+  } catch (...) {
+    return GS_ERR_ARG;
   }
   gs_param_list* l = new (std::nothrow) gs_param_list{current_device(), nullptr, 0, total};
   if (!l) return GS_ERR_ARG;

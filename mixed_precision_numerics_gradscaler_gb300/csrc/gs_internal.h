@@ -63,6 +63,15 @@ int current_device();
 // Records e as the calling thread's last CUDA error (gs_last_cuda_error).
 void record_cuda_error(cudaError_t e);
 
+// A byte range [lo, hi) of memory.
+struct Span {
+  uintptr_t lo, hi;
+};
+// True when two written ranges overlap each other, or a written range
+// overlaps a read one (empty ranges never do).  Sorts `writes` in place;
+// O((writes + reads) log writes).
+bool spans_conflict(Span* writes, size_t n_writes, const Span* reads, size_t n_reads);
+
 // Test hook (gs_test_set_stall): nonzero makes the TMA-fed kernels issue no
 // loads, so that their bounded waits run out.
 int test_stall();

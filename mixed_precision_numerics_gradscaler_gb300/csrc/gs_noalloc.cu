@@ -126,12 +126,15 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
     n_chunks += nc;
   }
   // The same per-pointer checks as gs_tensor_list_create and
-  // gs_unscale_check_update, applied to every pointer.
+  // gs_unscale_check_update, applied to every pointer; the ranges live on
+  // the stack (this entry point allocates nothing).
+  Span written[kNoAllocMaxTensors], read[kNoAllocMaxTensors];
   for (int32_t i = 0; i < tt.n; ++i) {
     const int64_t n = tt.numel[i];
     if (((uintptr_t)tt.in[i] & 1u) || ((uintptr_t)tt.out[i] & 3u)) return GS_ERR_ARG;
     const uintptr_t a = (uintptr_t)tt.in[i], b = (uintptr_t)tt.out[i];
-    if (a < b + (uintptr_t)n * 4 && b < a + (uintptr_t)n * 2) return GS_ERR_ARG;
+    written[i] = Span{b, b + (uintptr_t)n * 4};
+    read[i] = Span{a, a + (uintptr_t)n * 2};
     cudaPointerAttributes pa, pb;
     if (cudaPointerGetAttributes(&pa, tt.in[i]) != cudaSuccess ||
         cudaPointerGetAttributes(&pb, tt.out[i]) != cudaSuccess) {
@@ -145,6 +148,8 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
       if (!ok) return GS_ERR_ARG;
     }
   }
+  // no output may overlap any input or any other output
+  if (spans_conflict(written, (size_t)tt.n, read, (size_t)tt.n)) return GS_ERR_ARG;
   if (((uintptr_t)scale & 3u) || ((uintptr_t)growth_tracker & 3u) || ((uintptr_t)found_inf & 3u) ||
       (skipped && ((uintptr_t)skipped & 7u)))
     return GS_ERR_ARG;

@@ -277,3 +277,36 @@ def test_reciprocal_of_the_scale_for_many_scales(gs):
     torch.cuda.synchronize()
     assert_same_f32(got.cpu().numpy(), want, "fp32(1/S)")
     tl.close()
+
+
+def test_list_rejects_outputs_that_alias_another_tensor(gs):
+    """One launch covers the whole list, so an output may not overlap any
+    other tensor's input or output (rejected on the host, GS_ERR_ARG)."""
+    n = 4096
+    g = [torch.zeros(n, dtype=torch.float16, device=DEV) for _ in range(2)]
+    buf = torch.zeros(3 * n, dtype=torch.float32, device=DEV)
+    ok = gs.gs_tensor_list_create(g, [buf[:n], buf[n:2 * n]])   # disjoint: accepted
+    ok.close()
+    with pytest.raises(gs.GsError) as e:                         # two outputs overlap
+        gs.gs_tensor_list_create(g, [buf[:n], buf[n // 2:n // 2 + n]])
+    assert e.value.status == gs.GS_ERR_ARG
+    big = torch.zeros(4 * n, dtype=torch.float16, device=DEV)   # an output over another's input
+    g_in = big[:n]
+    out_over = big.view(torch.float32)[n // 4:n // 4 + n]
+    with pytest.raises(gs.GsError) as e:
+        gs.gs_tensor_list_create([g_in, g[1]], [buf[2 * n:], out_over])
+    assert e.value.status == gs.GS_ERR_ARG
+
+
+def test_param_list_rejects_masters_that_alias_another_tensor(gs):
+    n = 4096
+    w = torch.zeros(3 * n, dtype=torch.float32, device=DEV)
+    gr = [torch.zeros(n, dtype=torch.float32, device=DEV) for _ in range(2)]
+    gs.gs_param_list_create([w[:n], w[n:2 * n]], gr).close()                 # disjoint
+    with pytest.raises(gs.GsError):                                           # masters overlap
+        gs.gs_param_list_create([w[:n], w[n // 2:n // 2 + n]], gr)
+    with pytest.raises(gs.GsError):                                           # master over a grad
+        gs.gs_param_list_create([w[:n], gr[0]], [gr[0], gr[1]])
+    wb = torch.zeros(2 * n, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(gs.GsError):                                           # bf16 copies overlap
+        gs.gs_param_list_create([w[:n], w[n:2 * n]], gr, [wb[:n], wb[n // 2:n // 2 + n]])

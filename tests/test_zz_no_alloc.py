@@ -86,3 +86,19 @@ def test_noalloc_rejects_lists_beyond_its_fixed_array(gs):
     assert call(1, 16) == gs.GS_OK
     torch.cuda.synchronize()
     assert tracker.item() == 1
+
+
+def test_noalloc_rejects_outputs_that_alias_another_tensor(gs):
+    scale, tracker, found, skipped = _state(8.0)
+    n = 4096
+    g = [torch.zeros(n, dtype=torch.float16, device=DEV) for _ in range(2)]
+    buf = torch.zeros(2 * n, dtype=torch.float32, device=DEV)
+    with pytest.raises(gs.GsError) as e:
+        gs.gs_unscale_check_update_noalloc(g, [buf[:n], buf[n // 2:n // 2 + n]], scale, tracker,
+                                           found, skipped)
+    assert e.value.status == gs.GS_ERR_ARG
+    torch.cuda.synchronize()
+    assert tracker.item() == 0                 # nothing was launched
+    gs.gs_unscale_check_update_noalloc(g, [buf[:n], buf[n:]], scale, tracker, found, skipped)
+    torch.cuda.synchronize()
+    assert tracker.item() == 1
