@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
-    "unscale_check_update": ["unscale_check.cu", "gs_device.cuh", "gs_internal.h"],
+    "unscale_check_update": ["unscale_check.cu", "gs_device.cuh", "gs_layout.h"],
     "quant_1x128": ["fp8_quant.cu", "gs_device.cuh"],
     "dequant_1x128_bf16": ["fp8_dequant.cu", "gs_device.cuh"],
     "quant_128x128_tma": ["fp8_quant_tma.cu", "gs_device.cuh"],

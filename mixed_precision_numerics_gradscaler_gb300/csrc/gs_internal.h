@@ -5,50 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gs_layout.h"
+
 namespace gs {
-
-// One contiguous run of a gradient tensor: at most kChunkElems elements.
-// Chunk starts are multiples of kChunkElems from the tensor's start, so
-// every chunk of a tensor keeps the tensor's alignment.  A full chunk is
-// exactly one pass of a 256-thread CTA moving two 32-byte vectors (16 FP16
-// values each) per thread.
-struct Chunk {
-  const uint16_t* in;  // scaled FP16 gradients
-  float* out;          // FP32 unscaled output
-  int64_t n;
-};
-constexpr int64_t kChunkElems = 8192;
-
-// Per-list device workspace of the last-CTA epilogue.  Both words return
-// to zero at the end of every call.  A list created by
-// gs_tensor_list_create is followed by kUnscaleMaxCtas double slots for the
-// per-CTA sums of squares of the norm-computing form.
-struct ListWs {
-  unsigned int arrived;
-  int32_t found;
-  int32_t pad[2];
-};
-constexpr int kUnscaleCtasPerSm = 32;
-
-// One contiguous run of a parameter tensor for the master-weight update.
-struct MChunk {
-  float* w;            // fp32 master weights (updated in place)
-  uint16_t* w_bf16;    // bf16 copy for the forward pass, or nullptr
-  const float* g;      // unscaled fp32 gradients
-  int64_t n;
-};
-
-// Loss-scale policy applied by the last CTA of the unscale kernel.  With
-// hyst == nullptr it is the GradScaler loop; otherwise the hysteresis
-// policy: an overflow spends one unit of *hyst (S kept) until one is left,
-// then S = max(S * backoff, min_scale); a full clean window grows S and
-// restores *hyst (after every clean step when consecutive != 0).
-struct ScalerPolicy {
-  int32_t* hyst;
-  int32_t hysteresis;
-  int32_t consecutive;
-  float min_scale;
-};
 
 // Cached device properties of the current device.
 int sm_count();
