@@ -104,7 +104,8 @@ def _assert_exact(orc, got, want_f64, out_dtype, what):
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (300, 200, 1280),
                                    (1, 128, 128), (129, 1, 256), (130, 260, 640),
-                                   (2048, 2560, 256), (2181, 2304, 128)])
+                                   (2048, 2560, 256), (2181, 2304, 128), (1, 1, 128),
+                                   (5000, 8, 256), (64, 4096, 1024), (130, 40, 16384)])
 def test_gemm_exact_values_bit_exact(gs, orc, fmt, M, N, K):
     qa, sa, qb, sb = _exact_inputs(orc, fmt, M, N, K, seed=M * 7 + N * 3 + K + fmt)
     want = orc.gemm_fp8_block(qa, sa, qb, sb, fmt)
@@ -271,3 +272,12 @@ def test_quantise_then_gemm_pipeline(gs, orc, fmt):
     exact = orc.decode_array(xb, BF16).astype(np.float64) @ orc.decode_array(wb, BF16).astype(np.float64).T
     rel = np.linalg.norm(got - exact) / np.linalg.norm(exact)
     assert rel < (0.05 if fmt == E4M3 else 0.1)   # about 0.029 and 0.052 here
+
+
+def test_gemm_is_deterministic(gs, orc):
+    """The order of every addition is fixed (tensor-core partials per block,
+    then the promotion in increasing kb): two runs give the same bits."""
+    qa, sa, qb, sb = _general_inputs(orc, E4M3, 1000, 1536, 2048, seed=77)
+    a = _run(gs, qa, sa, qb, sb, E4M3, F32).cpu().numpy()
+    b = _run(gs, qa, sa, qb, sb, E4M3, F32).cpu().numpy()
+    assert (a.view(np.uint32) == b.view(np.uint32)).all()
