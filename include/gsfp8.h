@@ -328,7 +328,9 @@ int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C
  *       fp8_quant_block writes for block (1, 128));
  *   qb: row-major [N, K] codes (the weight stored [out, in]), sb:
  *       row-major [ceil(N / 128), K / 128] fp32 (block (128, 128));
- *   fmt: GS_E4M3 or GS_E5M2, the format of both operands;
+ *   fmt_a, fmt_b: GS_E4M3 or GS_E5M2, the formats of A and of B; they may
+ *      differ ([P5] "FP8 training": E4M3 for forward tensors, E5M2 for
+ *      gradients, so a backward GEMM multiplies E5M2 by E4M3);
  *   d: row-major [M, N], out_dtype GS_F32 or GS_BF16 (rounded to nearest
  *      even from the fp32 sum).
  * K % 128 == 0, M, N, K < 2^31 and fewer than 2^30 tiles of 128 x 256
@@ -340,8 +342,8 @@ int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C
  * accumulation error within one block.  A wait that runs out records
  * GS_ERR_TIMEOUT (gs_device_status) and leaves d unspecified. */
 int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
-                          int64_t M, int64_t N, int64_t K, int fmt, int out_dtype, void* d,
-                          void* stream);
+                          int64_t M, int64_t N, int64_t K, int fmt_a, int fmt_b, int out_dtype,
+                          void* d, void* stream);
 
 /* ------------------------------------------------------------------------
  * Diagnostics.

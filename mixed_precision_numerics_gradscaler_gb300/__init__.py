@@ -72,7 +72,7 @@ def _load_lib() -> ctypes.CDLL:
         "fp8_dequant_mx": (ci, [vp, vp, i64, i64, ci, ci, vp, vp]),
         "gs_unscale_check_update_noalloc": (ci, [vp, vp, vp, i32, vp, vp, vp, vp, f32, f32, i32, vp]),
         "gs_noalloc_limits": (ci, [ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64)]),
-        "fp8_gemm_block_scaled": (ci, [vp, vp, vp, vp, i64, i64, i64, ci, ci, vp, vp]),
+        "fp8_gemm_block_scaled": (ci, [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp, vp]),
         "gs_test_set_stall": (ci, [ci]),
     }
     for name, (res, args) in sigs.items():
@@ -353,8 +353,10 @@ def fp8_dequant_mx(q: torch.Tensor, scales: torch.Tensor, fmt, y: torch.Tensor, 
 
 
 def fp8_gemm_block_scaled(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
-                          fmt, d: torch.Tensor, stream=None) -> None:
-    """d[M, N] = block-scaled qa[M, K] @ qb[N, K]^T, promoted to fp32 every 128 of K."""
+                          fmt, d: torch.Tensor, stream=None, fmt_b=None) -> None:
+    """d[M, N] = block-scaled qa[M, K] @ qb[N, K]^T, promoted to fp32 every
+    128 of K. qa is in format `fmt`, qb in `fmt_b` (default: the same)."""
+    fmt_b = fmt if fmt_b is None else fmt_b
     for t, name in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb"), (d, "d")):
         _contig(t, name)
     M, K = qa.shape
@@ -363,7 +365,7 @@ def fp8_gemm_block_scaled(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, 
         raise ValueError(f"fp8_gemm_block_scaled: shapes qa {tuple(qa.shape)}, "
                          f"qb {tuple(qb.shape)}, d {tuple(d.shape)}")
     _check(_lib.fp8_gemm_block_scaled(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _FMTS[fmt],
-                                      _DTYPES[d.dtype], _ptr(d), _stream(stream)),
+                                      _FMTS[fmt_b], _DTYPES[d.dtype], _ptr(d), _stream(stream)),
            "fp8_gemm_block_scaled")
 
 

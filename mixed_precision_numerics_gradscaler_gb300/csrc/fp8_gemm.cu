@@ -146,10 +146,10 @@ __device__ __forceinline__ uint64_t umma_desc_k_sw128(uint32_t saddr) {
          (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f8f6f4: fp32 accumulator, A and B of the
-// given FP8 format (0 E4M3, 1 E5M2), both K-major, N = 256, M = 128.
-__host__ __device__ constexpr uint32_t umma_idesc_f8(uint32_t fmt) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kGBN >> 3) << 17) |
+// Instruction descriptor of kind::f8f6f4: fp32 accumulator, A and B each
+// of its own FP8 format (0 E4M3, 1 E5M2), both K-major, N = 256, M = 128.
+__host__ __device__ constexpr uint32_t umma_idesc_f8(uint32_t fmt_a, uint32_t fmt_b) {
+  return (1u << 4) | (fmt_a << 7) | (fmt_b << 10) | ((uint32_t)(kGBN >> 3) << 17) |
          ((uint32_t)(kGB >> 4) << 24);
 }
 
@@ -228,7 +228,7 @@ __device__ __forceinline__ void gemm_tile_coords(int t, int tiles_m, int tiles_n
   nt = r / rows;
 }
 
-template <int FMT, int OUT, bool TMA_STORE>
+template <int FA, int FB, int OUT, bool TMA_STORE>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_fp8_block_scaled(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       for (uint32_t j = it - issued_tail; j != it; ++j)
         g_drain(&full[j % kGStages], (j / kGStages) & 1u);
     } else if (warp == 1 && lane == 0) {  // MMA issuer
-      constexpr uint32_t idesc = umma_idesc_f8((uint32_t)FMT);
+      constexpr uint32_t idesc = umma_idesc_f8((uint32_t)FA, (uint32_t)FB);
       uint32_t it = 0;
       bool go = true;
       for (int t = blockIdx.x; go && t < n_tiles; t += gridDim.x) {
@@ -529,11 +529,11 @@ static CUresult encode_k_major(CUtensorMap* map, const uint8_t* base, int64_t ro
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int FMT, int OUT, bool TMA_STORE>
+template <int FA, int FB, int OUT, bool TMA_STORE>
 static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
                           const float* sa, const float* sb, int64_t M, int64_t N, int64_t K,
                           void* d, int32_t* status, cudaStream_t st) {
-  auto k = gemm_fp8_block_scaled<FMT, OUT, TMA_STORE>;
+  auto k = gemm_fp8_block_scaled<FA, FB, OUT, TMA_STORE>;
   // The setmaxnreg split is sized for exactly kGLaunchRegs per thread at
   // launch; a build that allocated another count must not run.
   static std::once_flag once;
@@ -555,13 +555,24 @@ static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   return cudaGetLastError();
 }
 
+template <int FA, int FB>
+static cudaError_t gemm_fmt(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                            const float* sa, const float* sb, int64_t M, int64_t N, int64_t K,
+                            bool f32, bool tma_store, void* d, int32_t* status, cudaStream_t st) {
+  if (tma_store)
+    return f32 ? gemm_t<FA, FB, GS_F32, true>(ma, mb, md, sa, sb, M, N, K, d, status, st)
+               : gemm_t<FA, FB, GS_BF16, true>(ma, mb, md, sa, sb, M, N, K, d, status, st);
+  return f32 ? gemm_t<FA, FB, GS_F32, false>(ma, mb, md, sa, sb, M, N, K, d, status, st)
+             : gemm_t<FA, FB, GS_BF16, false>(ma, mb, md, sa, sb, M, N, K, d, status, st);
+}
+
 // The caller has checked: qa and qb 16-byte aligned, K a multiple of 128,
 // M, N, K below 2^31 and fewer than 2^30 tiles.  Returns
 // cudaErrorNotSupported when the tensor-map entry point is missing.
 cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
-                                         const float* sb, int64_t M, int64_t N, int64_t K, int fmt,
-                                         int out_dtype, void* d, int32_t* status,
-                                         cudaStream_t st) {
+                                         const float* sb, int64_t M, int64_t N, int64_t K,
+                                         int fmt_a, int fmt_b, int out_dtype, void* d,
+                                         int32_t* status, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   const size_t esz = out_dtype == GS_F32 ? 4 : 2;
   if (K == 0) return cudaMemsetAsync(d, 0, (size_t)M * (size_t)N * esz, st);  // empty sums
@@ -587,15 +598,14 @@ cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, con
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const bool e4 = fmt == GS_E4M3, f32 = out_dtype == GS_F32;
-#define GS_GEMM_CALL(F, O, T) gemm_t<F, O, T>(ma, mb, md, sa, sb, M, N, K, d, status, st)
-  if (tma_store) {
-    if (e4) return f32 ? GS_GEMM_CALL(GS_E4M3, GS_F32, true) : GS_GEMM_CALL(GS_E4M3, GS_BF16, true);
-    return f32 ? GS_GEMM_CALL(GS_E5M2, GS_F32, true) : GS_GEMM_CALL(GS_E5M2, GS_BF16, true);
-  }
-  if (e4) return f32 ? GS_GEMM_CALL(GS_E4M3, GS_F32, false) : GS_GEMM_CALL(GS_E4M3, GS_BF16, false);
-  return f32 ? GS_GEMM_CALL(GS_E5M2, GS_F32, false) : GS_GEMM_CALL(GS_E5M2, GS_BF16, false);
-#undef GS_GEMM_CALL
+  const bool f32 = out_dtype == GS_F32, tma = tma_store != 0;
+  if (fmt_a == GS_E4M3)
+    return fmt_b == GS_E4M3
+               ? gemm_fmt<GS_E4M3, GS_E4M3>(ma, mb, md, sa, sb, M, N, K, f32, tma, d, status, st)
+               : gemm_fmt<GS_E4M3, GS_E5M2>(ma, mb, md, sa, sb, M, N, K, f32, tma, d, status, st);
+  return fmt_b == GS_E4M3
+             ? gemm_fmt<GS_E5M2, GS_E4M3>(ma, mb, md, sa, sb, M, N, K, f32, tma, d, status, st)
+             : gemm_fmt<GS_E5M2, GS_E5M2>(ma, mb, md, sa, sb, M, N, K, f32, tma, d, status, st);
 }
 
 }  // namespace gs

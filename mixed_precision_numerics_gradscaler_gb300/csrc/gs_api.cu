@@ -553,9 +553,10 @@ int fp8_dequant_mx(const uint8_t* q, const uint8_t* scales, int64_t R, int64_t C
 }
 
 int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
-                          int64_t M, int64_t N, int64_t K, int fmt, int out_dtype, void* d,
-                          void* stream) {
-  if (!valid_fmt(fmt) || !(out_dtype == GS_F32 || out_dtype == GS_BF16)) return GS_ERR_DTYPE;
+                          int64_t M, int64_t N, int64_t K, int fmt_a, int fmt_b, int out_dtype,
+                          void* d, void* stream) {
+  if (!valid_fmt(fmt_a) || !valid_fmt(fmt_b) || !(out_dtype == GS_F32 || out_dtype == GS_BF16))
+    return GS_ERR_DTYPE;
   if (M < 0 || N < 0 || K < 0 || K % 128 != 0 || M >= (1LL << 31) || K >= (1LL << 31) ||
       N >= (1LL << 31) || !mul_ok(M, N) || !mul_ok(M * N, 4) || !mul_ok(M, K) || !mul_ok(N, K))
     return GS_ERR_SHAPE;
@@ -580,8 +581,8 @@ int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
   }
   int32_t* status = device_status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
-  cudaError_t e = launch_gemm_fp8_block_scaled(qa, sa, qb, sb, M, N, K, fmt, out_dtype, d, status,
-                                               static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_gemm_fp8_block_scaled(qa, sa, qb, sb, M, N, K, fmt_a, fmt_b, out_dtype, d,
+                                               status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
 

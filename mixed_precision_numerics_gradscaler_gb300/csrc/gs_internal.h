@@ -64,9 +64,9 @@ cudaError_t launch_quant_tensor_delayed(const void* x, int dtype, int64_t n, int
                                         float* history, int hist_len, int32_t* pos,
                                         float* scale_used, uint32_t* partials, cudaStream_t stream);
 cudaError_t launch_gemm_fp8_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
-                                         const float* sb, int64_t M, int64_t N, int64_t K, int fmt,
-                                         int out_dtype, void* d, int32_t* status,
-                                         cudaStream_t stream);
+                                         const float* sb, int64_t M, int64_t N, int64_t K,
+                                         int fmt_a, int fmt_b, int out_dtype, void* d,
+                                         int32_t* status, cudaStream_t stream);
 cudaError_t launch_set_state(float* scale, int32_t* tracker, float h_scale, int32_t h_tracker,
                              cudaStream_t stream);
 

@@ -87,8 +87,10 @@ def _load():
             "orc_sum_squares": (ctypes.c_double, [vp, i64]),
             "orc_clip_coef": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
             "orc_master_update_sgd": (None, [vp, vp, vp, i64, ctypes.c_float, ctypes.c_float, i32]),
-            "orc_gemm_fp8_block_elem": (ctypes.c_double, [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int]),
-            "orc_gemm_fp8_block": (None, [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]),
+            "orc_gemm_fp8_block_elem": (ctypes.c_double, [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int,
+                                                          ctypes.c_int]),
+            "orc_gemm_fp8_block": (None, [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                          vp]),
             "orc_e8m0_decode": (ctypes.c_double, [ctypes.c_uint8]),
             "orc_mx_scale_code": (i32, [ctypes.c_double, ctypes.c_int]),
             "orc_quant_mx": (None, [vp, ctypes.c_int, i64, i64, ctypes.c_int, vp, vp]),
@@ -360,18 +362,22 @@ def master_update_sgd(w: np.ndarray, g: np.ndarray, lr: float, coef: float, foun
 
 # ---- block-scaled FP8 GEMM ----------------------------------------------------
 
-def gemm_fp8_block(qa, sa, qb, sb, fmt: int = E4M3) -> np.ndarray:
+def gemm_fp8_block(qa, sa, qb, sb, fmt: int = E4M3, fmt_b: int | None = None) -> np.ndarray:
     """A codes [M, K] with 1x128 scales [M, K/128]; B codes [N, K] with
-    128x128 scales [N/128, K/128] -> D [M, N] (float64)."""
+    128x128 scales [N/128, K/128] -> D [M, N] (float64). A is in format
+    `fmt`, B in `fmt_b` (default: the same)."""
+    fmt_b = fmt if fmt_b is None else fmt_b
     qa, qb = np.ascontiguousarray(qa, np.uint8), np.ascontiguousarray(qb, np.uint8)
     sa, sb = np.ascontiguousarray(sa, np.float32), np.ascontiguousarray(sb, np.float32)
     M, K = qa.shape
     N = qb.shape[0]
     d = np.empty((M, N), np.float64)
-    _load().orc_gemm_fp8_block(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, fmt, _ptr(d))
+    _load().orc_gemm_fp8_block(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, fmt, fmt_b, _ptr(d))
     return d
 
 
-def gemm_fp8_block_elem(qa, sa, qb, sb, m: int, n: int, fmt: int = E4M3) -> float:
+def gemm_fp8_block_elem(qa, sa, qb, sb, m: int, n: int, fmt: int = E4M3,
+                        fmt_b: int | None = None) -> float:
+    fmt_b = fmt if fmt_b is None else fmt_b
     return _load().orc_gemm_fp8_block_elem(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), qa.shape[1],
-                                           m, n, fmt)
+                                           m, n, fmt, fmt_b)

@@ -115,9 +115,10 @@ void   orc_master_update_sgd(float* w, uint16_t* w_bf16, const float* g, int64_t
  *      ([P1] "FP8 needs a finer-grained fix"; [P5] "FP8 training"; see
  *      gemm.c) ------------------------------------------------------------ */
 double orc_gemm_fp8_block_elem(const uint8_t* qa, const float* sa, const uint8_t* qb,
-                               const float* sb, int64_t K, int64_t m, int64_t n, int fmt);
+                               const float* sb, int64_t K, int64_t m, int64_t n, int fmt_a,
+                               int fmt_b);
 void orc_gemm_fp8_block(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
-                        int64_t M, int64_t N, int64_t K, int fmt, double* d);
+                        int64_t M, int64_t N, int64_t K, int fmt_a, int fmt_b, double* d);
 
 /* Pieces of the block path, exposed so tests can pin each step. */
 float orc_amax(const void* x, int dtype, int64_t n);          /* NaN-propagating */

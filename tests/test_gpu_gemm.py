@@ -53,35 +53,35 @@ def _codes_of(orc, fmt, values):
     return out
 
 
-def _exact_inputs(orc, fmt, M, N, K, seed):
+def _exact_inputs(orc, fmt, M, N, K, seed, fmt_b=None):
     rng = np.random.default_rng(seed)
-    cmap = _codes_of(orc, fmt, [-2.0, -1.0, 0.0, 1.0, 2.0])
-    lut = np.array([cmap[v] for v in (-2.0, -1.0, 0.0, 1.0, 2.0)], np.uint8)
-    qa = lut[rng.integers(0, 5, (M, K))]
-    qb = lut[rng.integers(0, 5, (N, K))]
+    vals = (-2.0, -1.0, 0.0, 1.0, 2.0)
+    lut = lambda f: np.array([_codes_of(orc, f, vals)[v] for v in vals], np.uint8)
+    qa = lut(fmt)[rng.integers(0, 5, (M, K))]
+    qb = lut(fmt if fmt_b is None else fmt_b)[rng.integers(0, 5, (N, K))]
     nkb = K // 128
     sa = np.exp2(rng.integers(-2, 3, (M, nkb))).astype(np.float32)
     sb = np.exp2(rng.integers(-2, 3, ((N + 127) // 128, nkb))).astype(np.float32)
     return qa, sa, qb, sb
 
 
-def _general_inputs(orc, fmt, M, N, K, seed):
+def _general_inputs(orc, fmt, M, N, K, seed, fmt_b=None):
     rng = np.random.default_rng(seed)
-    codes = _finite_codes(orc, fmt)
-    qa = codes[rng.integers(0, len(codes), (M, K))]
-    qb = codes[rng.integers(0, len(codes), (N, K))]
+    ca, cb = _finite_codes(orc, fmt), _finite_codes(orc, fmt if fmt_b is None else fmt_b)
+    qa = ca[rng.integers(0, len(ca), (M, K))]
+    qb = cb[rng.integers(0, len(cb), (N, K))]
     nkb = K // 128
     sa = rng.lognormal(-4.0, 2.0, (M, nkb)).astype(np.float32)
     sb = rng.lognormal(-6.0, 2.0, ((N + 127) // 128, nkb)).astype(np.float32)
     return qa, sa, qb, sb
 
 
-def _run(gs, qa, sa, qb, sb, fmt, out_dtype):
+def _run(gs, qa, sa, qb, sb, fmt, out_dtype, fmt_b=None):
     M, N = qa.shape[0], qb.shape[0]
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
     d = torch.full((M, N), float("nan"), dtype=torch.float32 if out_dtype == F32 else torch.bfloat16,
                    device=DEV)
-    gs.fp8_gemm_block_scaled(t(qa), t(sa), t(qb), t(sb), fmt, d)
+    gs.fp8_gemm_block_scaled(t(qa), t(sa), t(qb), t(sb), fmt, d, fmt_b=fmt_b)
     torch.cuda.synchronize()
     assert gs.gs_device_status() == 0
     return d
@@ -144,8 +144,8 @@ def test_gemm_exact_values_store_paths(gs, orc, M, N, K, out, offset):
         assert torch.isnan(buf[:offset]).all()  # nothing written before D
 
 
-def _tolerance(orc, qa, sa, qb, sb, fmt):
-    absd = orc.gemm_fp8_block(qa & 0x7F, sa, qb & 0x7F, sb, fmt)
+def _tolerance(orc, qa, sa, qb, sb, fmt, fmt_b=None):
+    absd = orc.gemm_fp8_block(qa & 0x7F, sa, qb & 0x7F, sb, fmt, fmt_b)
     nkb = qa.shape[1] // 128
     return (2.0 ** -24 * (nkb + 3) + E_BLK) * absd
 
@@ -281,3 +281,23 @@ def test_gemm_is_deterministic(gs, orc):
     a = _run(gs, qa, sa, qb, sb, E4M3, F32).cpu().numpy()
     b = _run(gs, qa, sa, qb, sb, E4M3, F32).cpu().numpy()
     assert (a.view(np.uint32) == b.view(np.uint32)).all()
+
+
+@pytest.mark.parametrize("fa,fb", [(E5M2, E4M3), (E4M3, E5M2)])
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (300, 200, 1280), (2181, 2304, 128)])
+def test_gemm_mixed_formats_exact_values(gs, orc, fa, fb, M, N, K):
+    """E5M2 gradients times E4M3 weights (a backward GEMM, "Mixed precision
+    and FP8 training", "FP8 training") and the reverse: bit-exact."""
+    qa, sa, qb, sb = _exact_inputs(orc, fa, M, N, K, seed=M + N + K + 3 * fa + fb, fmt_b=fb)
+    want = orc.gemm_fp8_block(qa, sa, qb, sb, fa, fb)
+    got = _run(gs, qa, sa, qb, sb, fa, F32, fmt_b=fb)
+    _assert_exact(orc, got, want, F32, f"mixed {fa}x{fb} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fa,fb", [(E5M2, E4M3), (E4M3, E5M2)])
+def test_gemm_mixed_formats_general_codes_within_bound(gs, orc, fa, fb):
+    qa, sa, qb, sb = _general_inputs(orc, fa, 256, 256, 1024, seed=9 + fa, fmt_b=fb)
+    want = orc.gemm_fp8_block(qa, sa, qb, sb, fa, fb)
+    tol = _tolerance(orc, qa, sa, qb, sb, fa, fb)
+    got = _run(gs, qa, sa, qb, sb, fa, F32, fmt_b=fb).cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all() and (np.abs(got - want) <= tol).all()

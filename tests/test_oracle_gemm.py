@@ -9,23 +9,26 @@ def _decode(orc, q):
     return orc.fp8_decode_array(q, E4M3).astype(np.float64)
 
 
-def test_gemm_matches_library_matmul_blockwise(orc):
+@pytest.mark.parametrize("fa,fb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_gemm_matches_library_matmul_blockwise(orc, fa, fb):
+    """Both formats, also mixed (E5M2 gradients times E4M3 weights in a
+    backward GEMM, "Mixed precision and FP8 training", "FP8 training")."""
     rng = np.random.default_rng(0)
     M, N, K = 64, 256, 384
-    qa = rng.integers(0, 256, (M, K)).astype(np.uint8)
-    qb = rng.integers(0, 256, (N, K)).astype(np.uint8)
-    qa[qa & 0x7F == 0x7F] = 0                      # no NaN codes
-    qb[qb & 0x7F == 0x7F] = 0
+    finite = lambda f: np.flatnonzero(np.isfinite(orc.fp8_decode_array(np.arange(256, dtype=np.uint8), f)))
+    qa = finite(fa)[rng.integers(0, len(finite(fa)), (M, K))].astype(np.uint8)
+    qb = finite(fb)[rng.integers(0, len(finite(fb)), (N, K))].astype(np.uint8)
     sa = rng.uniform(0.1, 10, (M, K // 128)).astype(np.float32)
     sb = rng.uniform(0.1, 10, (N // 128, K // 128)).astype(np.float32)
-    d = orc.gemm_fp8_block(qa, sa, qb, sb)
-    A, B = _decode(orc, qa), _decode(orc, qb)
+    d = orc.gemm_fp8_block(qa, sa, qb, sb, fa, fb)
+    A = orc.fp8_decode_array(qa, fa).astype(np.float64)
+    B = orc.fp8_decode_array(qb, fb).astype(np.float64)
     ref = np.zeros((M, N))
     for kb in range(K // 128):
         part = A[:, kb * 128:(kb + 1) * 128] @ B[:, kb * 128:(kb + 1) * 128].T
         ref += part * sa[:, kb:kb + 1].astype(np.float64) * np.repeat(sb[:, kb], 128)[None, :].astype(np.float64)
     assert np.allclose(d, ref, rtol=1e-12, atol=0)
-    assert orc.gemm_fp8_block_elem(qa, sa, qb, sb, 5, 200) == d[5, 200]
+    assert orc.gemm_fp8_block_elem(qa, sa, qb, sb, 5, 200, fa, fb) == d[5, 200]
 
 
 def test_gemm_one_hot_rows_pick_weight_rows(orc):

@@ -68,6 +68,8 @@ MUTANTS = {
         "w[i] = fmaf(-lr, coef * g[i], w[i]);"),
     "GEMM weight scale indexed by row instead of block": (
         "gemm.c", "(double)sb[(n / 128) * nkb + kb]", "(double)sb[n * nkb + kb]"),
+    "GEMM decodes B in A's format": (
+        "gemm.c", "orc_fp8_decode(qb[n * K + k], fmt_b)", "orc_fp8_decode(qb[n * K + k], fmt_a)"),
     "GEMM promotion with one block's scale for all": (
         "gemm.c", "(double)sa[m * nkb + kb]", "(double)sa[m * nkb]"),
     "dequant scale index transposed": (
