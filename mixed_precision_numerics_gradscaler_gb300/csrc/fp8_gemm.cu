@@ -9,9 +9,11 @@
 //   D[m][n] = sum_kb sa[m][kb] * sb[n/128][kb] * sum_{k in kb} A[m][k] * B[n][k]
 //
 // A = [M, K] and B = [N, K] FP8 codes (both K-major, as fp8_quant_block
-// writes them), D = [M, N] fp32 or bf16.  Persistent CTAs (one per SM) walk
+// writes them; each operand E4M3 or E5M2, the tensor cores take mixed
+// pairs), D = [M, N] fp32 or bf16.  Persistent CTAs (one per SM) walk
 // 128 x 256 tiles of D in groups of kGroupM tile rows (so the A and B panels
-// in use at once stay in L2); each CTA is warp-specialised:
+// in use at once stay in L2).  Each CTA has three warpgroups; setmaxnreg
+// moves registers from the first (40 each) to the other two (232 each):
 //   warp 0 (one lane)  TMA loads of the 128 x 128-byte A tile and the
 //                      256 x 128-byte B tile of each K-block (128-byte
 //                      swizzle, no multicast) into a 4-stage ring;
@@ -20,14 +22,20 @@
 //                      (M 128, N 256, K 32) into one of two TMEM
 //                      accumulators, then commits to the stage's "empty"
 //                      barrier and the accumulator's "full" barrier;
-//   warps 2-9          each reads one 32-row x 128-column quarter of the
+//   warps 2-3          idle (they complete the first warpgroup);
+//   warps 4-11         each reads one 32-row x 128-column quarter of the
 //                      block's fp32 partial from TMEM (tcgen05.ld: warp w
 //                      sees TMEM lanes 32 (w % 4) ...), multiplies by
 //                      sa * sb and adds into fp32 registers (packed fp32x2
 //                      fma: the promotion), releasing the accumulator as
 //                      soon as its last TMEM read completes; after the
-//                      tile's last K-block it stores its 32 x 128 piece of D
+//                      tile's last K-block it stages its 32 x 128 piece of
+//                      D in shared memory and writes it with TMA stores
 //                      while the tensor cores already work on the next tile.
+// Every wait is bounded by %globaltimer: a role that gives up records
+// GS_ERR_TIMEOUT, raises a shared abort flag so the others leave their
+// loops, waits (bounded) for its own loads or MMAs in flight, and the TMEM
+// columns are freed on every path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
