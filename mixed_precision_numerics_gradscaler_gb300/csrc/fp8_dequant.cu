@@ -5,8 +5,10 @@
 // an FP16 value: cvt.rn.f16x2.{e4m3x2,e5m2x2}); the product is one fp32
 // rounding; the BF16 form rounds that product to nearest even.
 //
-// One thread handles 16 codes (one 16-byte load) -> 64 B of fp32 or 32 B of
-// bf16.  Scale lookup: 1x128 -> scales[e / 128]; 128x128 ->
+// dequant_v8 (32-byte aligned codes and output): one thread handles 32
+// codes (one 32-byte load) -> 128 B of fp32 or 64 B of bf16 in 32-byte
+// stores; dequant_v (16-byte aligned): 16 codes per thread; dequant_any:
+// one element per thread.  Scale lookup: 1x128 -> scales[e / 128]; 128x128 ->
 // scales[(row / 128) * (C / 128) + col / 128]; per-tensor -> scales[0].
 #include <cuda_runtime.h>
 #include <stdint.h>

@@ -7,6 +7,12 @@
 // "Failure 1": per-tensor current scaling).
 //
 // Kernels:
+//   quant_1x128_v8x2 -- BF16/FP16 input, 32-byte aligned (the usual case):
+//                       one 4-lane group per 1x128 tile, two 32-byte loads
+//                       and one 32-byte store of codes per lane, amax by a
+//                       2-step shuffle on magnitude bit patterns.
+//   quant_1x128_v8   -- same input, 32-byte aligned x but 16-byte codes: one
+//                       8-lane group per tile.
 //   quant_1x128_v16  -- BF16/FP16 input, 16-byte aligned: one 16-lane group
 //                       per 1x128 tile (8 elements per lane), amax by a
 //                       4-step shuffle on magnitude bit patterns.
