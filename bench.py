@@ -12,9 +12,13 @@ synthetic inputs resident in HBM:
 value = algorithmic HBM bytes of the step / device time (GB/s).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--sweep] [--no-e2e]
+                       [--sweep] [--no-e2e] [--only KERNEL]
 Under torchrun (N > 1) every rank runs its own replica of the step on its
 own GPU (no data-path collective); rank 0 prints one JSON line.
+--impl reference times the CPU oracle on the host threads (the pages ship no
+implementation); --sweep runs the 1 MiB .. 8 GiB bandwidth sweep; --only
+times one kernel alone (the rows beyond the step, and the FP8 GEMM in
+TFLOP/s against the FP8 tensor peak).
 """
 from __future__ import annotations
 
