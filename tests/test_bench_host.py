@@ -1,0 +1,68 @@
+"""Host-side pieces of bench.py on CPU: the clock-record parser, the choice
+of FP8 peak, the staleness rule of the recorded DRAM traffic, and the
+threaded oracle runner."""
+import json
+import threading
+
+import bench
+
+
+def _sampler(lines):
+    c = bench.ClockSampler("0")
+    c.lines = lines
+    return c.summary()
+
+
+def test_clock_summary_uses_loaded_samples_and_reports_throttle_reasons():
+    idle = "1500, 2070, 120.5, Not Active, Not Active, Not Active, Not Active"
+    busy = "2070, 2070, 950.0, Not Active, Not Active, Not Active, Not Active"
+    capped = "1605, 2070, 1390.0, Not Active, Not Active, Not Active, Active"
+    s = _sampler([idle, busy, busy, capped, "garbage", "1, 2, three, a, b, c, d"])
+    assert s["samples"] == 3                      # the idle sample is not "under load"
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["power_w_max"] == 1390.0
+    hot = "1800, 2070, 1000.0, Active, Not Active, Active, Not Active"
+    assert _sampler([hot])["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert _sampler([]) is None
+    # no sample above the load threshold: all samples count
+    assert _sampler([idle])["samples"] == 1
+
+
+def test_fp8_peak_is_sustained_for_long_loops(tmp_path, monkeypatch):
+    peaks = tmp_path / "peaks.json"
+    peaks.write_text(json.dumps({"bf16_tflops": 1932.5, "bf16_tflops_sustained": 1759.5}))
+    monkeypatch.setattr(bench, "PEAKS_FILE", str(peaks))
+    assert bench.fp8_peak(0.1) == (3865.0, "measured bf16_tflops x 2")
+    assert bench.fp8_peak(2.0) == (3519.0, "measured bf16_tflops_sustained x 2")
+    monkeypatch.setattr(bench, "PEAKS_FILE", str(tmp_path / "absent.json"))
+    assert bench.fp8_peak(0.1)[1].startswith("fallback")
+
+
+def test_recorded_traffic_is_dropped_when_the_kernel_sources_change(tmp_path, monkeypatch):
+    rec = tmp_path / "traffic.json"
+    key = "dequant_1x128_bf16"
+    rec.write_text(json.dumps({key: {"dram_bytes_per_launch": 123, "sources_sha": bench.sources_sha(key)}}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(rec))
+    assert bench.measured_traffic(key) == 123
+    rec.write_text(json.dumps({key: {"dram_bytes_per_launch": 123, "sources_sha": "0" * 16}}))
+    assert bench.measured_traffic(key) is None
+    assert bench.measured_traffic("no_such_kernel") is None
+
+
+def test_oracle_parallel_runs_exactly_the_requested_steps():
+    class Counter:
+        def __init__(self):
+            self.n, self.lock, self.threads = 0, threading.Lock(), set()
+
+        def run(self):
+            with self.lock:
+                self.n += 1
+                self.threads.add(threading.get_ident())
+
+    c = Counter()
+    runs, el = bench.oracle_parallel(c, 4, reps=37)
+    assert runs == 37 and c.n == 37 and el >= 0.0
+    c2 = Counter()
+    runs, el = bench.oracle_parallel(c2, 3, seconds=0.05)
+    assert runs == c2.n >= 1 and el >= 0.05
