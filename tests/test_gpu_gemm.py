@@ -301,3 +301,19 @@ def test_gemm_mixed_formats_general_codes_within_bound(gs, orc, fa, fb):
     tol = _tolerance(orc, qa, sa, qb, sb, fa, fb)
     got = _run(gs, qa, sa, qb, sb, fa, F32, fmt_b=fb).cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all() and (np.abs(got - want) <= tol).all()
+
+
+def test_gemm_random_shapes_bit_exact(gs, orc):
+    """40 seeded random shapes (M, N in 1..700, K in 128..1024), random
+    operand formats (mixed pairs too) and output types, exact-value inputs:
+    every one bit-exact against the oracle."""
+    rng = np.random.default_rng(2024)
+    for i in range(40):
+        M, N = (int(v) for v in rng.integers(1, 701, 2))
+        K = 128 * int(rng.integers(1, 9))
+        fa, fb = (int(v) for v in rng.integers(0, 2, 2))
+        out = F32 if rng.integers(0, 2) else BF16
+        qa, sa, qb, sb = _exact_inputs(orc, fa, M, N, K, seed=100 + i, fmt_b=fb)
+        want = orc.gemm_fp8_block(qa, sa, qb, sb, fa, fb)
+        got = _run(gs, qa, sa, qb, sb, fa, out, fmt_b=fb)
+        _assert_exact(orc, got, want, out, f"case {i}: {M}x{N}x{K} fmt {fa}/{fb} out {out}")
