@@ -366,3 +366,24 @@ def test_exhaustive_fp32_cast_at_unit_scale(gs, orc, fmt):
             want = oracle_codes(bits)
             bad = np.nonzero(got != want)[0]
             assert bad.size == 0, [(hex(int(bits[i])), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def test_block_quant_random_cases(gs, orc):
+    """30 seeded random cases of the block quantiser and dequantiser: block
+    shape, rows and columns, input type, format, special values, and input
+    and code buffers at random offsets (so the vector, TMA and scalar paths
+    all run) -- bit for bit against the oracle."""
+    rng = np.random.default_rng(77)
+    for i in range(30):
+        br = int(rng.choice([1, 128]))
+        R = int(rng.integers(1, 4)) * (128 if br == 128 else int(rng.integers(1, 90)))
+        C = 128 * int(rng.integers(1, 6))
+        dt = str(rng.choice(["bf16", "f16", "f32"]))
+        fmt = str(rng.choice(["e4m3", "e5m2"]))
+        xh, xd = _host_input(rng, R, C, dt, special=bool(rng.integers(0, 2)))
+        x_off = int(rng.choice([0, 1, 8, 16]))
+        if x_off:
+            big = torch.zeros(R * C + x_off, dtype=xd.dtype, device=DEV)
+            big[x_off:] = xd.reshape(-1)
+            xd = big[x_off:].view(R, C)
+        _check_block(gs, orc, xh, xd, dt, br, 128, fmt, q_off=int(rng.choice([0, 1, 8, 16])))

@@ -310,3 +310,31 @@ def test_param_list_rejects_masters_that_alias_another_tensor(gs):
     wb = torch.zeros(2 * n, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(gs.GsError):                                           # bf16 copies overlap
         gs.gs_param_list_create([w[:n], w[n:2 * n]], gr, [wb[:n], wb[n // 2:n // 2 + n]])
+
+
+def test_random_lists_views_and_scales(gs, orc):
+    """30 seeded random gradient lists (1-12 tensors of 0..40000 elements,
+    each viewed at a random element offset into its own buffers), random
+    scales (powers of two and arbitrary), sometimes a planted Inf/NaN: every
+    output, flag and scaler field against the oracle."""
+    rng = np.random.default_rng(31)
+    for case in range(30):
+        n_t = int(rng.integers(1, 13))
+        sizes = [int(v) for v in rng.integers(0, 40001, n_t)]
+        hosts = [(rng.standard_normal(n) * np.exp(rng.uniform(-8, 8))).astype(np.float16).view(np.uint16)
+                 for n in sizes]
+        if rng.integers(0, 3) == 0 and sum(sizes) > 0:
+            t = int(rng.choice([i for i, n in enumerate(sizes) if n > 0]))
+            hosts[t][int(rng.integers(0, sizes[t]))] = int(rng.choice([0x7C00, 0xFC00, 0x7E00]))
+        grads, outs = [], []
+        for h in hosts:
+            gi, go = int(rng.integers(0, 9)), int(rng.integers(0, 9))
+            bi = torch.zeros(h.size + 8, dtype=torch.float16, device=DEV)
+            bo = torch.zeros(h.size + 8, dtype=torch.float32, device=DEV)
+            g = bi[gi:gi + h.size]
+            if h.size:
+                g.copy_(to_dev16(h, torch.float16))
+            grads.append(g)
+            outs.append(bo[go:go + h.size])
+        S = float(2.0 ** int(rng.integers(-20, 30))) if rng.integers(0, 2) else float(rng.uniform(0.1, 1e6))
+        _run_list(gs, orc, hosts, S, views=(grads, outs))
