@@ -139,3 +139,37 @@ def test_printed_master_weight_demo_on_the_device(gs):
     assert f"{w[0].item():.4f}" == g["fp32_weight_after"]
     assert f"{wb[0].float().item():.4f}" == "2.0000"
     pl.close()
+
+
+def test_master_update_random_lists(gs, orc):
+    """20 seeded random parameter lists (1-8 tensors of 1..50000 elements),
+    learning rate, clipping threshold, bf16 copy or not, and sometimes an
+    overflowed step: the update against the oracle given the same norm."""
+    rng = np.random.default_rng(606)
+    for case in range(20):
+        sizes = [int(v) for v in rng.integers(1, 50001, int(rng.integers(1, 9)))]
+        w_host = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+        g_host = [(rng.standard_normal(n) * np.exp(rng.uniform(-6, 2))).astype(np.float32) for n in sizes]
+        w = [torch.from_numpy(x.copy()).to(DEV) for x in w_host]
+        g = [torch.from_numpy(x).to(DEV) for x in g_host]
+        with_bf16 = bool(rng.integers(0, 2))
+        wb = [torch.zeros(n, dtype=torch.bfloat16, device=DEV) for n in sizes] if with_bf16 else None
+        lr = float(rng.uniform(1e-5, 0.5))
+        max_norm = float(rng.choice([0.0, float(rng.uniform(0.01, 100.0))]))
+        found_v = int(rng.integers(0, 5) == 0)
+        norm_v = float(np.float32(orc.grad_norm(g_host)))
+        norm = torch.tensor([norm_v], dtype=torch.float32, device=DEV)
+        found = torch.tensor([found_v], dtype=torch.int32, device=DEV)
+        pl = gs.gs_param_list_create(w, g, wb)
+        gs.gs_master_update_sgd(pl, lr, max_norm, norm, found)
+        torch.cuda.synchronize()
+        coef = orc.clip_coef(norm_v, max_norm)
+        for i in range(len(sizes)):
+            ref_w = w_host[i].copy()
+            ref_b = orc.master_update_sgd(ref_w, g_host[i], lr, coef, found_v)
+            assert_same_f32(w[i].cpu().numpy(), ref_w, f"case {case} tensor {i}")
+            if with_bf16 and not found_v:
+                assert same_bf16(bits_of(wb[i]), ref_b).all(), f"case {case} tensor {i} bf16"
+            if with_bf16 and found_v:
+                assert (bits_of(wb[i]) == 0).all()           # a skipped step writes nothing
+        pl.close()

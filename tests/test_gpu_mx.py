@@ -155,3 +155,18 @@ def test_mx_cfg3_full_size_sampled(gs, orc):
     assert_same_bytes(q.view(-1)[ii].cpu().numpy(), rq.reshape(-1), "cfg3 mx codes")
     assert_same_bytes(s.view(-1)[bi].cpu().numpy(), rs.reshape(-1), "cfg3 mx scales")
     assert same_bf16(bits_of(y.view(-1)[ii]), ry.reshape(-1)).all()
+
+
+def test_mx_random_cases(gs, orc):
+    """30 seeded random MXFP8 cases (rows, columns in multiples of 32, input
+    type, format, code and output offsets): quantise and dequantise bit for
+    bit against the oracle."""
+    rng = np.random.default_rng(404)
+    for i in range(30):
+        R = int(rng.integers(3, 80))
+        C = 32 * int(rng.integers(1, 40))
+        dt = str(rng.choice(["bf16", "f16", "f32"]))
+        fmt = str(rng.choice(["e4m3", "e5m2"]))
+        xh, xd = _input(rng, R, C, dt)
+        _check(gs, orc, xh, xd, dt, fmt, q_off=int(rng.choice([0, 1, 16, 32])),
+               y_off=int(rng.choice([0, 1, 4, 8])))

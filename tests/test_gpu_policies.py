@@ -169,3 +169,29 @@ def test_hysteresis_min_scale_and_reduction_to_gradscaler(gs, orc):
         seen.append(scale.item())
     assert seen == [4.0, 2.0, 1.0, 1.0, 1.0]
     tl.close()
+
+
+def test_delayed_random_histories(gs, orc):
+    """20 seeded random runs of delayed scaling: tensor length, history
+    length, input type and format random; six steps each (spike, NaN and
+    recovery) against the oracle's ring, scale and codes."""
+    rng = np.random.default_rng(505)
+    for case in range(20):
+        n = int(rng.integers(1, 200000))
+        H = int(rng.integers(1, 40))
+        dt = str(rng.choice(["bf16", "f16", "f32"]))
+        fmt = str(rng.choice(["e4m3", "e5m2"]))
+        ref = orc.DelayedScaling(H)
+        hist = torch.zeros(H, dtype=torch.float32, device=DEV)
+        pos = torch.zeros(1, dtype=torch.int32, device=DEV)
+        used = torch.empty(1, dtype=torch.float32, device=DEV)
+        ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=DEV)
+        for k, (xh, xd) in enumerate(_steps(rng, n, dt)):
+            q = torch.empty(n, dtype=torch.uint8, device=DEV)
+            gs.fp8_quant_tensor_delayed(xd, fmt, q, hist, pos, used, ws)
+            rq, rs = ref.quant(xh, FMT[fmt], dtype=ODT[dt])
+            torch.cuda.synchronize()
+            assert_same_bytes(q.cpu().numpy(), rq, f"case {case} step {k} codes")
+            assert_same_f32(used.cpu().numpy(), np.array([rs], np.float32), f"case {case} step {k}")
+            assert_same_f32(hist.cpu().numpy(), ref.history, f"case {case} step {k} history")
+            assert int(pos.item()) == ref.pos.value
