@@ -56,3 +56,23 @@ def test_clip_coefficient(orc):
     n = orc.grad_norm([g])
     c = orc.clip_coef(np.float32(n), 1.0)
     assert abs(np.linalg.norm((np.float32(c) * g).astype(np.float64)) - 1.0) < 1e-6
+
+
+def test_bf16_copy_is_the_library_round_to_nearest_even_cast(orc):
+    """The forward copy ("Mixed precision and FP8 training", "Range and
+    precision": FP32 master weights converted to bf16 each step) is the
+    updated fp32 weight rounded to nearest even -- torch's own bf16 cast,
+    including values halfway between two bf16 numbers."""
+    import torch
+    rng = np.random.default_rng(8)
+    w = rng.standard_normal(200_000).astype(np.float32)
+    # plant exact halfway cases (low 16 bits 0x8000) with even and odd bf16 parents
+    w.view(np.uint32)[:1000] = (w.view(np.uint32)[:1000] & 0xFFFF0000) | 0x8000
+    g = np.zeros_like(w)                      # zero gradient: the weight is unchanged
+    out = orc.master_update_sgd(w, g, 0.1, 1.0, 0)
+    lib = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert (out == lib).all()
+    g = rng.standard_normal(w.size).astype(np.float32)
+    out = orc.master_update_sgd(w, g, 0.01, 1.0, 0)
+    lib = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert (out == lib).all()

@@ -72,6 +72,13 @@ MUTANTS = {
         "gemm.c", "orc_fp8_decode(qb[n * K + k], fmt_b)", "orc_fp8_decode(qb[n * K + k], fmt_a)"),
     "GEMM promotion with one block's scale for all": (
         "gemm.c", "(double)sa[m * nkb + kb]", "(double)sa[m * nkb]"),
+    "MX all-zero block scaled by 2^0": (
+        "mx_quant.c", "    e = -127;\n  } else {", "    e = 0;\n  } else {"),
+    "bf16 master copy truncated": (
+        "master.c", "w_bf16[i] = orc_bf16_encode(w[i]);",
+        "w_bf16[i] = (uint16_t)(*(const uint32_t*)&w[i] >> 16);"),
+    "GEMM activation scale of the next K-block": (
+        "gemm.c", "(double)sa[m * nkb + kb]", "(double)sa[m * nkb + (kb + 1) % nkb]"),
     "dequant scale index transposed": (
         "fp8_quant.c", "float s = scales[(r / br) * nbc + c / bc];", "float s = scales[(c / bc) * (R / br) + r / br];"),
 }
