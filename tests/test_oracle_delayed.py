@@ -108,3 +108,21 @@ def test_window_1000_probes_twice_as_eagerly_as_2000(orc):
         ds.update(0, 2.0, 0.5, 1000, 2, False, 1.0)
         pt.update(0, 2.0, 0.5, 2000)
     assert ds.scale.value == 2.0 ** 18 and pt.scale.value == 2.0 ** 17
+
+
+def test_history_is_a_ring_of_the_last_amax_values(orc):
+    """After k steps the history holds the amax of the last H tensors, each
+    in slot (step index mod H), and the position is k mod H ("Why FP8
+    training is stable", "Failure 1": a short history of recent max-abs
+    values)."""
+    H = 4
+    d = orc.DelayedScaling(H)
+    amaxes = [3.0, 0.5, 7.0, 2.0, 1.0, 0.25]
+    for k, a in enumerate(amaxes):
+        x = np.array([a, -a / 2, 0.0], np.float32)
+        d.quant(x, E4M3)
+        assert d.pos.value == (k + 1) % H
+    want = np.zeros(H, np.float32)
+    for k, a in enumerate(amaxes):
+        want[k % H] = a
+    assert (d.history == want).all()

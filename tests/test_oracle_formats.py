@@ -302,3 +302,18 @@ def test_swamping_threshold_2048(orc):
     assert orc.f16_encode(np.float32(1.0 + 2.0 ** -11)) == one
     assert orc.f16_encode(np.float32(1.0 + 2.0 ** -11 + 2.0 ** -20)) == one + 1
     assert orc.f16_encode(np.float32(1.0 + 3 * 2.0 ** -11)) == one + 2   # tie from odd -> up
+
+
+def test_nan_encodes_to_a_nan_in_every_format(orc):
+    """Every NaN input (either sign, quiet or signalling payload) encodes to a
+    NaN pattern -- all-ones exponent, non-zero mantissa -- in FP16 and BF16
+    (which payload is not part of the result), and to 0x7F in FP8."""
+    pats = np.array([0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF812345, 0x7FFFFFFF], np.uint32)
+    x = pats.view(np.float32)
+    f16 = orc.encode_array(x, 0)
+    assert (((f16 & 0x7C00) == 0x7C00) & ((f16 & 0x03FF) != 0)).all()
+    bf16 = orc.encode_array(x, 1)
+    assert (((bf16 & 0x7F80) == 0x7F80) & ((bf16 & 0x007F) != 0)).all()
+    assert np.isnan(orc.decode_array(f16, 0)).all() and np.isnan(orc.decode_array(bf16, 1)).all()
+    for fmt in (0, 1):
+        assert (orc.fp8_encode_array(x, fmt) == 0x7F).all()

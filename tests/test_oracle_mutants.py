@@ -79,6 +79,19 @@ MUTANTS = {
         "w_bf16[i] = (uint16_t)(*(const uint32_t*)&w[i] >> 16);"),
     "GEMM activation scale of the next K-block": (
         "gemm.c", "(double)sa[m * nkb + kb]", "(double)sa[m * nkb + (kb + 1) % nkb]"),
+    "unscale by S instead of 1/S": (
+        "gradscaler.c", "out[i] = (float)v * inv_scale;", "out[i] = (float)v * scale;"),
+    "backoff by the growth factor": (
+        "gradscaler.c", "*scale = *scale * backoff_factor;", "*scale = *scale * growth_factor;"),
+    "delayed history max ignores NaN": (
+        "delayed.c", "if (isnan(history[j])) hnan = 1;", "if (0) hnan = 1;"),
+    "delayed amax recorded before the step's cast reads it": (
+        "delayed.c", "*pos = (*pos + 1) % hist_len;", "*pos = (*pos + 2) % hist_len;"),
+    "MX exponent from the rounded-up log2": (
+        "mx_quant.c", "e = (k - 1) - emax_elem(fmt);", "e = k - emax_elem(fmt);"),
+    "bf16 quiet NaN pattern of f16": (
+        "fp_formats.c", "orc_bf16_encode(float f) { return (uint16_t)encode_ieee(f, &FMT_BF16, 0x7FC0u); }",
+        "orc_bf16_encode(float f) { return (uint16_t)encode_ieee(f, &FMT_BF16, 0x7E00u); }"),
     "dequant scale index transposed": (
         "fp8_quant.c", "float s = scales[(r / br) * nbc + c / bc];", "float s = scales[(c / bc) * (R / br) + r / br];"),
 }
