@@ -13,6 +13,7 @@
 #include <stdint.h>
 
 #include "gs_device.cuh"
+#include "gs_quant.cuh"
 #include "gs_internal.h"
 
 namespace gs {
@@ -60,35 +61,24 @@ __global__ void __launch_bounds__(kDelThreads)
   int64_t v = tid;
   for (; v + nthreads < nv; v += 2 * nthreads) {
     const V8 a = ld_stream8(x + 32 * v), b = ld_stream8(x + 32 * (v + nthreads));
-    uint32_t pa[4], pb[4];
+    uint32_t in[16], c[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.w[2 * j] & mm, a.w[2 * j + 1] & mm),
-                                 __vmaxu2(b.w[2 * j] & mm, b.w[2 * j + 1] & mm)));
-      pa[j] = quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j]), lo16<Tag>(a.w[2 * j]), s, r, fin) |
-              (quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j + 1]), lo16<Tag>(a.w[2 * j + 1]), s, r,
-                                       fin)
-               << 16);
-      pb[j] = quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j]), lo16<Tag>(b.w[2 * j]), s, r, fin) |
-              (quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j + 1]), lo16<Tag>(b.w[2 * j + 1]), s, r,
-                                       fin)
-               << 16);
+    for (int j = 0; j < 8; ++j) {
+      m2 = __vmaxu2(m2, __vmaxu2(a.w[j] & mm, b.w[j] & mm));
+      in[j] = a.w[j];
+      in[8 + j] = b.w[j];
     }
-    st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(pa[0], pa[1], pa[2], pa[3]));
-    st_stream(reinterpret_cast<uint4*>(q + 16 * (v + nthreads)), make_uint4(pb[0], pb[1], pb[2], pb[3]));
+    quant_words<Tag, FMT, 16>(in, c, s, r);
+    st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(c[0], c[1], c[2], c[3]));
+    st_stream(reinterpret_cast<uint4*>(q + 16 * (v + nthreads)), make_uint4(c[4], c[5], c[6], c[7]));
   }
   for (; v < nv; v += nthreads) {
     const V8 a = ld_stream8(x + 32 * v);
-    uint32_t pa[4];
+    uint32_t c[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      m2 = __vmaxu2(m2, __vmaxu2(a.w[2 * j] & mm, a.w[2 * j + 1] & mm));
-      pa[j] = quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j]), lo16<Tag>(a.w[2 * j]), s, r, fin) |
-              (quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j + 1]), lo16<Tag>(a.w[2 * j + 1]), s, r,
-                                       fin)
-               << 16);
-    }
-    st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(pa[0], pa[1], pa[2], pa[3]));
+    for (int j = 0; j < 4; ++j) m2 = __vmaxu2(m2, __vmaxu2(a.w[2 * j] & mm, a.w[2 * j + 1] & mm));
+    quant_words<Tag, FMT, 8>(a.w, c, s, r);
+    st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(c[0], c[1], c[2], c[3]));
   }
   uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
   // ragged tail (n not a multiple of 16)
@@ -159,24 +149,23 @@ __global__ void __launch_bounds__(kDelThreads)
 template <int DT, int FMT>
 static cudaError_t delayed_t(const void* x, int64_t n, uint8_t* q, float* history, int hist_len,
                              int32_t* pos, float* scale_used, uint32_t* partials, cudaStream_t st) {
+  // One CTA per 8192 elements, at most 16 per SM (more than fit at once:
+  // CTAs of later waves even out the SMs, measured faster than one
+  // persistent wave) and at most kMaxAmaxBlocks partials.
+  bool vec = false;
+  if constexpr (DT != GS_F32) vec = ((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 15u) == 0;
+  using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
   int64_t grid = (n + kDelThreads * 32 - 1) / (kDelThreads * 32);
-  const int64_t cap = (int64_t)sm_count() * 8;
+  const int64_t cap = (int64_t)sm_count() * 16;
   if (grid > cap) grid = cap;
   if (grid > kMaxAmaxBlocks) grid = kMaxAmaxBlocks;
   if (grid < 1) grid = 1;
-  if constexpr (DT != GS_F32) {
-    if (((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 15u) == 0) {
-      using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
-      quant_delayed_v8<Tag, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(
-          reinterpret_cast<const uint8_t*>(x), n, q, history, hist_len, scale_used, partials);
-    } else {
-      quant_delayed_any<DT, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(x, n, q, history, hist_len,
-                                                                         scale_used, partials);
-    }
-  } else {
+  if (vec)
+    quant_delayed_v8<Tag, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(
+        reinterpret_cast<const uint8_t*>(x), n, q, history, hist_len, scale_used, partials);
+  else
     quant_delayed_any<DT, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(x, n, q, history, hist_len,
                                                                        scale_used, partials);
-  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   delayed_record<DT><<<1, kDelThreads, 0, st>>>(partials, (int)grid, history, hist_len, pos);

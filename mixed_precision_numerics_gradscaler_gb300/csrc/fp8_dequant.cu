@@ -134,7 +134,7 @@ static cudaError_t dequant_t(const uint8_t* q, const float* scales, int64_t R, i
   if (vec8 && n >= 32) {
     const int64_t n32 = n / 32;
     int64_t grid = (n32 + kDeqThreads - 1) / kDeqThreads;
-    const int64_t cap8 = (int64_t)sm_count() * 32;
+    const int64_t cap8 = (int64_t)sm_count() * 64;  // several waves: measured best of 32-128
     if (grid > cap8) grid = cap8;
     dequant_v8<KIND, FMT, OUT><<<(unsigned)grid, kDeqThreads, 0, st>>>(
         q, scales, n32, C, reinterpret_cast<uint8_t*>(y));

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kMxThreads)
 
 static int64_t mx_grid(int64_t work) {
   int64_t grid = (work + kMxThreads - 1) / kMxThreads;
-  const int64_t cap = (int64_t)sm_count() * 16;
+  const int64_t cap = (int64_t)sm_count() * 64;  // several waves: measured best of 16-128
   return grid > cap ? cap : (grid < 1 ? 1 : grid);
 }
 

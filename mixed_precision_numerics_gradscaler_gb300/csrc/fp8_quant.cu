@@ -27,6 +27,7 @@
 #include <stdint.h>
 
 #include "gs_device.cuh"
+#include "gs_quant.cuh"
 #include "gs_internal.h"
 
 namespace gs {
@@ -92,13 +93,11 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
-      const bool fin = isfinite(s);
       const float r = __frcp_rn(s);
-      uint2 o;
-      o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].x), lo16<Tag>(v[u].x), s, r, fin) |
-            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].y), lo16<Tag>(v[u].y), s, r, fin) << 16);
-      o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].z), lo16<Tag>(v[u].z), s, r, fin) |
-            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].w), lo16<Tag>(v[u].w), s, r, fin) << 16);
+      const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t c[2];
+      quant_words<Tag, FMT, 4>(in, c, s, r);
+      const uint2 o = make_uint2(c[0], c[1]);
       if (t < n_tiles) {
         st_stream(q + t * 16 + l16, o);
         if (l16 == 0) scales[t] = s;
@@ -150,15 +149,9 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
-      const bool fin = isfinite(s);
       const float r = __frcp_rn(s);
       uint32_t c[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        c[j] = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].w[2 * j]), lo16<Tag>(v[u].w[2 * j]), s, r, fin) |
-               (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[u].w[2 * j + 1]), lo16<Tag>(v[u].w[2 * j + 1]), s, r,
-                                fin)
-                << 16);
+      quant_words<Tag, FMT, 8>(v[u].w, c, s, r);
       if (t < n_tiles) {
         st_stream16(q + t * 128 + l8 * 16, make_uint4(c[0], c[1], c[2], c[3]));
         if (l8 == 0) scales[t] = s;
@@ -181,7 +174,6 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t n_slots = (n_tiles + 7) >> 3;
-  constexpr int kSteps = QuotSteps<Tag>::value;
   // uniform loop bound across the warp: every lane reaches the shuffles
   for (int64_t p0 = warp; p0 < n_slots; p0 += n_warps) {
     const int64_t t = 8 * p0 + grp;
@@ -201,23 +193,89 @@ __global__ void __launch_bounds__(kQuantThreads)
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
-    const bool fin = isfinite(s);
     const float r = __frcp_rn(s);
-    V8 o;
+    uint32_t in[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      o.w[j] = quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j]), lo16<Tag>(a.w[2 * j]), s, r, fin) |
-               (quant_pair<FMT, kSteps>(hi16<Tag>(a.w[2 * j + 1]), lo16<Tag>(a.w[2 * j + 1]), s, r,
-                                        fin)
-                << 16);
-      o.w[4 + j] =
-          quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j]), lo16<Tag>(b.w[2 * j]), s, r, fin) |
-          (quant_pair<FMT, kSteps>(hi16<Tag>(b.w[2 * j + 1]), lo16<Tag>(b.w[2 * j + 1]), s, r, fin)
-           << 16);
+    for (int j = 0; j < 8; ++j) {
+      in[j] = a.w[j];
+      in[8 + j] = b.w[j];
     }
+    V8 o;
+    quant_words<Tag, FMT, 16>(in, o.w, s, r);
     if (t < n_tiles) {
       st_stream8(q + t * 128 + l4 * 32, o);
       if (l4 == 0) scales[t] = s;
+    }
+  }
+}
+
+// ---- 128x128, 16-bit input, direct 32-byte loads -----------------------------
+// One 512-thread CTA per 128x128 block at a time, grid-stride over the blocks
+// with three CTAs resident per SM.  Thread t loads the 32-byte chunk t mod 8
+// of rows t/8 and t/8 + 64 of the block (a warp reads four whole 256-byte
+// rows per load instruction), so the block sits in registers, 32 elements per
+// thread.  Block amax: packed magnitude max, warp shuffles, one word per warp
+// in shared memory (two sets, alternating by block, so one barrier per block
+// suffices), read back by every thread as four 16-byte vectors.  Codes leave
+// as two 16-byte stores per thread.  Measured against a TMA-staged form of
+// the same block walk (2-3 stages of 32 KB per CTA, two or three CTAs per SM),
+// this one moves more bytes per second: forty-eight resident warps per SM
+// hide the per-block amax-then-cast chain better than a deeper load queue.
+constexpr int kQ128Threads = 512;
+constexpr int kQ128Warps = kQ128Threads / 32;
+constexpr int kQ128RowStep = kQ128Threads / 8;  // 64: rows between a thread's two loads
+
+template <typename Tag, int FMT>
+__global__ void __launch_bounds__(kQ128Threads, 3)
+    quant_128x128_v8(const uint8_t* __restrict__ x, int64_t nbr, int64_t nbc,
+                     uint8_t* __restrict__ q, int64_t C, float* __restrict__ scales) {
+  __shared__ __align__(16) uint32_t red[2][kQ128Warps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = tid & 7, row = tid >> 3;
+  const int64_t n_blocks = nbr * nbc;
+  if ((int64_t)blockIdx.x >= n_blocks) return;
+  const int64_t row_bytes = C * 2;
+  // block b = blockIdx.x + k * gridDim.x is (b / nbc, b % nbc); both advance
+  // by gridDim.x's quotient and remainder, so the loop divides nothing
+  const int64_t step_r = gridDim.x / nbc, step_c = gridDim.x % nbc;
+  int64_t br = blockIdx.x / nbc, bc = blockIdx.x % nbc;
+  int par = 0;
+  for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x, par ^= 1) {
+    const uint8_t* xb = x + (br * 128 + row) * row_bytes + bc * 256 + chunk * 32;
+    const V8 a = ld_stream8(xb), c = ld_stream8(xb + kQ128RowStep * row_bytes);
+    const uint32_t mm = 0x7FFF7FFFu;
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m2 = __vmaxu2(m2, __vmaxu2(a.w[j] & mm, c.w[j] & mm));
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red[par][warp] = m;
+    __syncthreads();
+    {
+      const uint4* r4 = reinterpret_cast<const uint4*>(red[par]);
+      uint4 v = r4[0];
+#pragma unroll
+      for (int w = 1; w < kQ128Warps / 4; ++w) {
+        const uint4 u = r4[w];
+        v = make_uint4(max(v.x, u.x), max(v.y, u.y), max(v.z, u.z), max(v.w, u.w));
+      }
+      m = max(max(v.x, v.y), max(v.z, v.w));
+    }
+    const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
+    const float r = __frcp_rn(s);
+    if (tid == 0) scales[b] = s;
+    uint32_t ca[4], cc[4];
+    quant_words<Tag, FMT, 8>(a.w, ca, s, r);
+    quant_words<Tag, FMT, 8>(c.w, cc, s, r);
+    uint8_t* qb = q + (br * 128 + row) * C + bc * 128 + chunk * 16;
+    st_stream(reinterpret_cast<uint4*>(qb), make_uint4(ca[0], ca[1], ca[2], ca[3]));
+    st_stream(reinterpret_cast<uint4*>(qb + kQ128RowStep * C), make_uint4(cc[0], cc[1], cc[2], cc[3]));
+    br += step_r;
+    bc += step_c;
+    if (bc >= nbc) {
+      bc -= nbc;
+      ++br;
     }
   }
 }
@@ -391,24 +449,24 @@ __global__ void __launch_bounds__(kQuantThreads)
       uint4 a[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) a[u] = ld_stream(x8 + v + u * nthreads);
+      uint32_t in[16], c[8];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        uint2 o;
-        o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].x), lo16<Tag>(a[u].x), s, r, fin) |
-              (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].y), lo16<Tag>(a[u].y), s, r, fin) << 16);
-        o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].z), lo16<Tag>(a[u].z), s, r, fin) |
-              (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a[u].w), lo16<Tag>(a[u].w), s, r, fin) << 16);
-        st_stream(q8 + v + u * nthreads, o);
+        in[4 * u] = a[u].x;
+        in[4 * u + 1] = a[u].y;
+        in[4 * u + 2] = a[u].z;
+        in[4 * u + 3] = a[u].w;
       }
+      quant_words<Tag, FMT, 16>(in, c, s, r);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) st_stream(q8 + v + u * nthreads, make_uint2(c[2 * u], c[2 * u + 1]));
     }
     for (; v < nv; v += nthreads) {
       const uint4 a = ld_stream(x8 + v);
-      uint2 o;
-      o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.x), lo16<Tag>(a.x), s, r, fin) |
-            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.y), lo16<Tag>(a.y), s, r, fin) << 16);
-      o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.z), lo16<Tag>(a.z), s, r, fin) |
-            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(a.w), lo16<Tag>(a.w), s, r, fin) << 16);
-      st_stream(q8 + v, o);
+      const uint32_t in[4] = {a.x, a.y, a.z, a.w};
+      uint32_t c[2];
+      quant_words<Tag, FMT, 4>(in, c, s, r);
+      st_stream(q8 + v, make_uint2(c[0], c[1]));
     }
     for (int64_t i = head + nv * 8 + tid; i < n; i += nthreads)
       q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
@@ -438,8 +496,10 @@ static cudaError_t quant_1x128_t(const void* x, int64_t R, int64_t C, uint8_t* q
     if ((xa & 31u) == 0 && (qa & 31u) == 0) {
       using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
       auto k = quant_1x128_v8x2<Tag, FMT>;
-      // oversubscribed grid: 16 CTAs per SM, each pass of a CTA moves 64 tiles
-      int64_t grid = (int64_t)sm_count() * 16;
+      // oversubscribed grid: 64 CTAs per SM (several waves; CTAs started late
+      // even out the SMs -- measured best of 16 to 128), each pass of a CTA
+      // moves 64 tiles
+      int64_t grid = (int64_t)sm_count() * 64;
       const int64_t need = (n_tiles + 8 * (kQuantThreads / 32) - 1) / (8 * (kQuantThreads / 32));
       if (grid > need) grid = need;
       if (grid < 1) grid = 1;
@@ -508,6 +568,32 @@ cudaError_t quant_128x128_simple_t(const void* x, int64_t R, int64_t C, uint8_t*
   return cudaGetLastError();
 }
 
+template <typename Tag, int FMT>
+static cudaError_t quant_128x128_v8_t(const void* x, int64_t R, int64_t C, uint8_t* q,
+                                      float* scales, cudaStream_t st) {
+  auto k = quant_128x128_v8<Tag, FMT>;
+  int occ = 0;
+  const cudaError_t e = kernel_blocks_per_sm((const void*)k, kQ128Threads, 0, &occ);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  const int64_t nbr = R / 128, nbc = C / 128;
+  int64_t grid = (int64_t)sm_count() * occ;
+  if (grid > nbr * nbc) grid = nbr * nbc;
+  k<<<(unsigned)grid, kQ128Threads, 0, st>>>(reinterpret_cast<const uint8_t*>(x), nbr, nbc, q, C,
+                                             scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_128x128_v8(const void* x, int dtype, int64_t R, int64_t C, int fmt,
+                                    uint8_t* q, float* scales, cudaStream_t st) {
+  if (R == 0 || C == 0) return cudaSuccess;
+  if (fmt == GS_E4M3)
+    return dtype == GS_BF16 ? quant_128x128_v8_t<BF16Tag, GS_E4M3>(x, R, C, q, scales, st)
+                            : quant_128x128_v8_t<F16Tag, GS_E4M3>(x, R, C, q, scales, st);
+  return dtype == GS_BF16 ? quant_128x128_v8_t<BF16Tag, GS_E5M2>(x, R, C, q, scales, st)
+                          : quant_128x128_v8_t<F16Tag, GS_E5M2>(x, R, C, q, scales, st);
+}
+
 cudaError_t launch_quant_128x128_simple(const void* x, int dtype, int64_t R, int64_t C, int fmt,
                                         uint8_t* q, float* scales, cudaStream_t st) {
   if (R == 0 || C == 0) return cudaSuccess;
@@ -531,7 +617,11 @@ static cudaError_t quant_tensor_t(const void* x, int64_t n, uint8_t* q, float* s
   k1<<<(unsigned)g1, kQuantThreads, 0, st>>>(x, n, partials);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t g2 = persistent_grid(k2, kQuantThreads * 8, n);
+  // pass 2 oversubscribes (32 CTAs per SM, several waves): measured faster
+  // than one persistent wave or 16 per SM, as CTAs of later waves even out
+  // the SMs; beyond 64 every CTA's reduction of the partials costs more
+  int64_t g2 = (n + kQuantThreads * 8 - 1) / (kQuantThreads * 8);
+  if (g2 > (int64_t)sm_count() * 32) g2 = (int64_t)sm_count() * 32;
   k2<<<(unsigned)g2, kQuantThreads, 0, st>>>(x, n, q, scale, partials, (int)g1);
   return cudaGetLastError();
 }

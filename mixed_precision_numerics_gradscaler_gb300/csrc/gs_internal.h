@@ -51,6 +51,13 @@ cudaError_t launch_quant_1x128(const void* x, int dtype, int64_t R, int64_t C, i
 cudaError_t launch_quant_128x128(const void* x, int dtype, int64_t R, int64_t C, int fmt,
                                  uint8_t* q, float* scales, int32_t* status,
                                  cudaStream_t stream);
+// The 128x128 kernels behind launch_quant_128x128: direct 32-byte loads
+// (16-bit input, x 32-byte and q 16-byte aligned), and one CTA per block for
+// any dtype and alignment.
+cudaError_t launch_quant_128x128_v8(const void* x, int dtype, int64_t R, int64_t C, int fmt,
+                                    uint8_t* q, float* scales, cudaStream_t stream);
+cudaError_t launch_quant_128x128_simple(const void* x, int dtype, int64_t R, int64_t C, int fmt,
+                                        uint8_t* q, float* scales, cudaStream_t stream);
 cudaError_t launch_quant_tensor(const void* x, int dtype, int64_t n, int fmt, uint8_t* q,
                                 float* scale, uint32_t* partials, cudaStream_t stream);
 cudaError_t launch_dequant(const uint8_t* q, const float* scales, int64_t R, int64_t C,

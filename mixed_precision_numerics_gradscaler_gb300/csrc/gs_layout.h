@@ -22,14 +22,18 @@ constexpr int64_t kChunkElems = 8192;
 
 // Per-list device workspace of the last-CTA epilogue.  Both words return
 // to zero at the end of every call.  A list created by
-// gs_tensor_list_create is followed by kUnscaleMaxCtas double slots for the
-// per-CTA sums of squares of the norm-computing form.
+// gs_tensor_list_create is followed by (SM count) x kUnscaleCtasPerSm double
+// slots for the per-CTA sums of squares of the norm-computing form.
 struct ListWs {
   unsigned int arrived;
   int32_t found;
   int32_t pad[2];
 };
-constexpr int kUnscaleCtasPerSm = 32;
+// CTAs per SM of the unscale grid (it walks the chunk table grid-stride):
+// several waves, so that CTAs started late even out the SMs' progress;
+// measured faster than 32 or 64 and, with the norm's per-CTA slots,
+// than 256.
+constexpr int kUnscaleCtasPerSm = 128;
 
 // One contiguous run of a parameter tensor for the master-weight update.
 struct MChunk {

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kMasterThreads)
 cudaError_t launch_master_update_sgd(const MChunk* d_chunks, int64_t n_chunks, float lr,
                                      float max_norm, const float* grad_norm,
                                      const int32_t* found_inf, cudaStream_t stream) {
-  int64_t grid = (int64_t)sm_count() * 16;
+  int64_t grid = (int64_t)sm_count() * 64;  // several waves: measured best of 16-128
   if (grid > n_chunks) grid = n_chunks;
   if (grid < 1) grid = 1;
   master_update_sgd_kernel<<<(unsigned)grid, kMasterThreads, 0, stream>>>(

@@ -1,6 +1,6 @@
 """The bounded device-side waits, exercised without a fault: a test hook
-makes the TMA-fed kernels (the 128x128 quantiser and the block-scaled FP8
-GEMM) issue no loads, so a barrier that nothing completes is waited on with
+makes the TMA-fed kernels (the TMA-staged 128x128 quantiser and the
+block-scaled FP8 GEMM) issue no loads, so a barrier that nothing completes is waited on with
 its limit. The kernel must give up after about 2 s, record GS_ERR_TIMEOUT
 in the device status word, free what it holds (the GEMM's tensor memory)
 and return, and the same context must then compute correctly again."""
@@ -66,7 +66,13 @@ def test_gemm_wait_runs_out_reports_timeout_and_recovers(gs, orc):
 def test_tma_quantiser_wait_runs_out_reports_timeout_and_recovers(gs, orc):
     rng = np.random.default_rng(9)
     xb = orc.encode_array(rng.standard_normal((256, 384)).astype(np.float64), 1)  # bf16 bits
-    x = torch.from_numpy(xb.view(np.int16)).to(DEV).view(torch.bfloat16)
+    # 16-byte but not 32-byte aligned input: the TMA-staged kernel's path
+    # (32-byte aligned input goes to the direct-load kernel, which has no
+    # wait to run out)
+    big = torch.zeros(256 * 384 + 8, dtype=torch.bfloat16, device=DEV)
+    big[8:] = torch.from_numpy(xb.view(np.int16)).to(DEV).view(torch.bfloat16).reshape(-1)
+    x = big[8:].view(256, 384)
+    assert x.data_ptr() % 32 == 16
     rq, rs = orc.quant_block(xb, 128, 128, E4M3, dtype=1)
     q = torch.empty(256, 384, dtype=torch.uint8, device=DEV)
     s = torch.empty(2, 3, dtype=torch.float32, device=DEV)
