@@ -622,6 +622,7 @@ static cudaError_t quant_tensor_t(const void* x, int64_t n, uint8_t* q, float* s
   // the SMs; beyond 64 every CTA's reduction of the partials costs more
   int64_t g2 = (n + kQuantThreads * 8 - 1) / (kQuantThreads * 8);
   if (g2 > (int64_t)sm_count() * 32) g2 = (int64_t)sm_count() * 32;
+  if (g2 < 1) g2 = 1;  // an empty tensor still gets its scale written
   k2<<<(unsigned)g2, kQuantThreads, 0, st>>>(x, n, q, scale, partials, (int)g1);
   return cudaGetLastError();
 }
