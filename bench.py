@@ -412,6 +412,39 @@ def _oracle_threads() -> int:
         return max(1, os.cpu_count() or 1)
 
 
+_ARM_PARTS = {0xd0c: "Arm Neoverse-N1", 0xd40: "Arm Neoverse-V1", 0xd49: "Arm Neoverse-N2",
+              0xd4f: "Arm Neoverse-V2"}
+
+
+def cpu_model(cpuinfo: str = None) -> str:
+    """The host CPU's name from /proc/cpuinfo: "model name" on x86; on Arm,
+    which lists only implementer and part numbers, the Arm part's name."""
+    if cpuinfo is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                cpuinfo = f.read()
+        except OSError:
+            return "unknown"
+    impl = part = None
+    for line in cpuinfo.splitlines():
+        key, _, val = line.partition(":")
+        key, val = key.strip().lower(), val.strip()
+        if key == "model name" and val:
+            return val
+        if key == "cpu implementer" and impl is None:
+            impl = val
+        if key == "cpu part" and part is None:
+            part = val
+    if impl and part:
+        try:
+            if int(impl, 16) == 0x41 and int(part, 16) in _ARM_PARTS:
+                return _ARM_PARTS[int(part, 16)]
+        except ValueError:
+            pass
+        return f"implementer {impl} part {part}"
+    return "unknown"
+
+
 def oracle_parallel(sample, threads: int, seconds: float = None, reps: int = None):
     """Runs sample.run() on `threads` host threads (the oracle is plain C
     behind ctypes, which releases the GIL; the inputs are shared read-only)
@@ -452,7 +485,7 @@ def cpu_baseline(seconds: float) -> dict:
     repsn, eln = oracle_parallel(sample, n, seconds=seconds / 2)
     single = throughput(sample.bytes * reps1, el1)
     return {"value": throughput(sample.bytes * repsn, eln), "unit": UNIT, "cores": n,
-            "kind": "oracle", "single_thread_value": single,
+            "kind": "oracle", "single_thread_value": single, "cpu_model": cpu_model(),
             "sample": f"{sample.desc}; {repsn} runs in {eln:.1f} s on {n} host threads "
                       f"({reps1} runs in {el1:.1f} s on one thread: {single:.3f} {UNIT})"}
 
@@ -477,7 +510,7 @@ def run_reference(args):
                        "pages ship no implementation; steps spread over the host threads",
                        "sample_bytes_per_step": sample.bytes},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle",
-                             "sample": sample.desc},
+                             "cpu_model": cpu_model(), "sample": sample.desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

@@ -66,3 +66,14 @@ def test_oracle_parallel_runs_exactly_the_requested_steps():
     c2 = Counter()
     runs, el = bench.oracle_parallel(c2, 3, seconds=0.05)
     assert runs == c2.n >= 1 and el >= 0.05
+
+
+def test_cpu_model_names_x86_and_arm_hosts():
+    x86 = "processor\t: 0\nvendor_id\t: GenuineIntel\nmodel name\t: Intel(R) Xeon(R) Platinum 8480+\n"
+    assert bench.cpu_model(x86) == "Intel(R) Xeon(R) Platinum 8480+"
+    grace = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\nCPU part\t: 0xd4f\n"
+    assert bench.cpu_model(grace) == "Arm Neoverse-V2"
+    other = "CPU implementer\t: 0x61\nCPU part\t: 0x023\n"
+    assert bench.cpu_model(other) == "implementer 0x61 part 0x023"
+    assert bench.cpu_model("") == "unknown"
+    assert isinstance(bench.cpu_model(), str)
