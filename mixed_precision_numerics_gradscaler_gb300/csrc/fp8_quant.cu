@@ -18,10 +18,16 @@
 //                       4-step shuffle on magnitude bit patterns.
 //   quant_1x128_v32  -- FP32 input, aligned: one warp per tile.
 //   quant_1x128_any  -- any dtype / alignment: one warp per tile, scalar.
+//   quant_128x128_v8 -- BF16/FP16 input, 32-byte aligned (codes 16-byte):
+//                       one 512-thread CTA per 128x128 block, the block
+//                       held in registers (two 32-byte loads per thread).
 //   quant_128x128_any-- any dtype / alignment: one CTA per block, two
 //                       passes over the block (the second hits L2).  The
-//                       TMA-staged 128x128 kernel lives in fp8_quant_tma.cu.
+//                       TMA-staged 128x128 kernel (16-byte aligned input)
+//                       lives in fp8_quant_tma.cu.
 //   amax_partials + quant_tensor -- the two passes of per-tensor scaling.
+// The 16-bit paths cast through quant_words (gs_quant.cuh): the exact
+// quotient on f32x2 pairs.
 // All paths are HBM-bound: 1x128 moves 2 + 1 + 4/128 bytes per BF16 element.
 #include <cuda_runtime.h>
 #include <stdint.h>
