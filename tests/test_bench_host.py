@@ -77,3 +77,22 @@ def test_cpu_model_names_x86_and_arm_hosts():
     assert bench.cpu_model(other) == "implementer 0x61 part 0x023"
     assert bench.cpu_model("") == "unknown"
     assert isinstance(bench.cpu_model(), str)
+
+
+def test_reference_arm_prints_one_complete_line(monkeypatch, capsys):
+    """`bench.py --impl reference` at rank 0: the CPU oracle on the bounded
+    sample of the step, one JSON line with the contract's keys."""
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1"]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 2
+    assert d["config"]["workload"] == bench.WORKLOAD
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["sample"] and cb["cpu_model"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
