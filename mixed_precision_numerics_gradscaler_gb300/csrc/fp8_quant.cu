@@ -16,18 +16,22 @@
 //   quant_1x128_v16  -- BF16/FP16 input, 16-byte aligned: one 16-lane group
 //                       per 1x128 tile (8 elements per lane), amax by a
 //                       4-step shuffle on magnitude bit patterns.
-//   quant_1x128_v32  -- FP32 input, aligned: one warp per tile.
+//   quant_1x128_f32_v8 -- FP32 input, 32-byte aligned (codes 16-byte): one
+//                       8-lane group per tile, two 32-byte loads per lane.
+//   quant_1x128_v32  -- FP32 input, 16-byte aligned: one warp per tile.
 //   quant_1x128_any  -- any dtype / alignment: one warp per tile, scalar.
 //   quant_128x128_v8 -- BF16/FP16 input, 32-byte aligned (codes 16-byte):
 //                       one 512-thread CTA per 128x128 block, the block
-//                       held in registers (two 32-byte loads per thread).
+//                       held in registers (two 32-byte loads per thread);
+//                       quant_128x128_f32_v8 the same for FP32 (four loads,
+//                       codes 8-byte aligned).
 //   quant_128x128_any-- any dtype / alignment: one CTA per block, two
 //                       passes over the block (the second hits L2).  The
 //                       TMA-staged 128x128 kernel (16-byte aligned input)
 //                       lives in fp8_quant_tma.cu.
 //   amax_partials + quant_tensor -- the two passes of per-tensor scaling.
-// The 16-bit paths cast through quant_words (gs_quant.cuh): the exact
-// quotient on f32x2 pairs.
+// The vector paths cast through quant_words / quant_words_f32
+// (gs_quant.cuh): the exact quotient on f32x2 pairs.
 // All paths are HBM-bound: 1x128 moves 2 + 1 + 4/128 bytes per BF16 element.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -286,6 +290,117 @@ __global__ void __launch_bounds__(kQ128Threads, 3)
   }
 }
 
+// ---- 128x128, FP32 input, direct 32-byte loads ---------------------------------
+// The FP32 form of quant_128x128_v8: a block row is 512 bytes, so thread t
+// loads the 32-byte chunk t mod 16 of rows t/16 + 32 i, i < 4 (a warp reads
+// two whole rows per load instruction), 32 elements per thread; codes leave
+// as four 8-byte stores per thread (a warp writes two 128-byte code rows).
+constexpr int kQ128F32RowStep = kQ128Threads / 16;  // 32
+
+template <int FMT>
+__global__ void __launch_bounds__(kQ128Threads, 2)
+    quant_128x128_f32_v8(const uint8_t* __restrict__ x, int64_t nbr, int64_t nbc,
+                         uint8_t* __restrict__ q, int64_t C, float* __restrict__ scales) {
+  __shared__ __align__(16) uint32_t red[2][kQ128Warps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = tid & 15, row = tid >> 4;
+  const int64_t n_blocks = nbr * nbc;
+  if ((int64_t)blockIdx.x >= n_blocks) return;
+  const int64_t row_bytes = C * 4;
+  const int64_t step_r = gridDim.x / nbc, step_c = gridDim.x % nbc;
+  int64_t br = blockIdx.x / nbc, bc = blockIdx.x % nbc;
+  int par = 0;
+  for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x, par ^= 1) {
+    const uint8_t* xb = x + (br * 128 + row) * row_bytes + bc * 512 + chunk * 32;
+    V8 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = ld_stream8(xb + i * kQ128F32RowStep * row_bytes);
+    const uint32_t mm = 0x7FFFFFFFu;
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = max(m, v[i].w[j] & mm);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red[par][warp] = m;
+    __syncthreads();
+    {
+      const uint4* r4 = reinterpret_cast<const uint4*>(red[par]);
+      uint4 u = r4[0];
+#pragma unroll
+      for (int w = 1; w < kQ128Warps / 4; ++w) {
+        const uint4 t4 = r4[w];
+        u = make_uint4(max(u.x, t4.x), max(u.y, t4.y), max(u.z, t4.z), max(u.w, t4.w));
+      }
+      m = max(max(u.x, u.y), max(u.z, u.w));
+    }
+    const float s = block_scale<FMT>(__uint_as_float(m));
+    const float r = __frcp_rn(s);
+    if (tid == 0) scales[b] = s;
+    uint8_t* qb = q + (br * 128 + row) * C + bc * 128 + chunk * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t c[2];
+      quant_words_f32<FMT, 8>(v[i].w, c, s, r);
+      st_stream(reinterpret_cast<uint2*>(qb + i * kQ128F32RowStep * C), make_uint2(c[0], c[1]));
+    }
+    br += step_r;
+    bc += step_c;
+    if (bc >= nbc) {
+      bc -= nbc;
+      ++br;
+    }
+  }
+}
+
+// ---- 1x128, FP32 input, 32-byte aligned: one 8-lane group per tile -----------
+// Each lane loads 16 elements (two adjacent 32-byte loads) of its tile, the
+// 8 lanes reduce the tile amax (integer max of fp32 magnitude patterns, three
+// shuffles), and each lane casts its 16 elements through quant_words_f32 and
+// writes one 16-byte store of codes.  A warp moves four tiles (2 KB in,
+// 512 B out) per slot.
+template <int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_1x128_f32_v8(const uint8_t* __restrict__ x, int64_t n_tiles, uint8_t* __restrict__ q,
+                       float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t n_slots = (n_tiles + 3) >> 2;
+  // uniform loop bound across the warp: every lane reaches the shuffles
+  for (int64_t p0 = warp; p0 < n_slots; p0 += n_warps) {
+    const int64_t t = 4 * p0 + grp;
+    V8 a, b;
+    if (t < n_tiles) {
+      a = ld_stream8(x + t * 512 + l8 * 64);
+      b = ld_stream8(x + t * 512 + l8 * 64 + 32);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a.w[j] = b.w[j] = 0;
+    }
+    const uint32_t mm = 0x7FFFFFFFu;
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, max(a.w[j] & mm, b.w[j] & mm));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float s = block_scale<FMT>(__uint_as_float(m));
+    const float r = __frcp_rn(s);
+    uint32_t in[16], c[4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      in[j] = a.w[j];
+      in[8 + j] = b.w[j];
+    }
+    quant_words_f32<FMT, 16>(in, c, s, r);
+    if (t < n_tiles) {
+      st_stream16(q + t * 128 + l8 * 16, make_uint4(c[0], c[1], c[2], c[3]));
+      if (l8 == 0) scales[t] = s;
+    }
+  }
+}
+
 // ---- 1x128, FP32 input, vectorised: one warp per tile ------------------------
 template <int FMT>
 __global__ void __launch_bounds__(kQuantThreads)
@@ -405,7 +520,28 @@ __global__ void __launch_bounds__(kQuantThreads)
     m = max(m, max(m2 & 0xFFFFu, m2 >> 16));
     for (int64_t i = head + nv * 8 + tid; i < n; i += nthreads) m = max(m, (uint32_t)(xs[i] & 0x7FFFu));
   } else {
-    for (int64_t i = tid; i < n; i += nthreads) m = max(m, mag_bits<DT>(x, i));
+    // 16-byte vectors of four fp32 once the pointer is aligned
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(x);
+    int64_t head = (int64_t)(((16u - ((uint32_t)(uintptr_t)xs & 15u)) & 15u) >> 2);
+    if (head > n) head = n;
+    const uint32_t mm = 0x7FFFFFFFu;
+    for (int64_t i = tid; i < head; i += nthreads) m = max(m, xs[i] & mm);
+    const int64_t nv = (n - head) >> 2;
+    const uint4* x4 = reinterpret_cast<const uint4*>(xs + head);
+    int64_t v = tid;
+    for (; v + 3 * nthreads < nv; v += 4 * nthreads) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = ld_stream(x4 + v + u * nthreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        m = max(m, max(max(a[u].x & mm, a[u].y & mm), max(a[u].z & mm, a[u].w & mm)));
+    }
+    for (; v < nv; v += nthreads) {
+      const uint4 a = ld_stream(x4 + v);
+      m = max(m, max(max(a.x & mm, a.y & mm), max(a.z & mm, a.w & mm)));
+    }
+    for (int64_t i = head + nv * 4 + tid; i < n; i += nthreads) m = max(m, xs[i] & mm);
   }
   m = warp_max(m);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -477,7 +613,42 @@ __global__ void __launch_bounds__(kQuantThreads)
     for (int64_t i = head + nv * 8 + tid; i < n; i += nthreads)
       q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
   } else {
-    for (int64_t i = tid; i < n; i += nthreads) q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
+    // 16-byte vectors of four fp32 -> four codes (one 4-byte store) where x
+    // is 16-byte and q 4-byte aligned at the same element
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(x);
+    int64_t head = (int64_t)(((16u - ((uint32_t)(uintptr_t)xs & 15u)) & 15u) >> 2);
+    if (head > n) head = n;
+    if ((((uintptr_t)(q + head)) & 3u) != 0) head = n;
+    for (int64_t i = tid; i < head; i += nthreads) q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
+    const int64_t nv = (n - head) >> 2;
+    const uint4* x4 = reinterpret_cast<const uint4*>(xs + head);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(q + head);
+    int64_t v = tid;
+    for (; v + 3 * nthreads < nv; v += 4 * nthreads) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = ld_stream(x4 + v + u * nthreads);
+      uint32_t in[16], c[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        in[4 * u] = a[u].x;
+        in[4 * u + 1] = a[u].y;
+        in[4 * u + 2] = a[u].z;
+        in[4 * u + 3] = a[u].w;
+      }
+      quant_words_f32<FMT, 16>(in, c, s, r);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q4[v + u * nthreads] = c[u];
+    }
+    for (; v < nv; v += nthreads) {
+      const uint4 a = ld_stream(x4 + v);
+      const uint32_t in[4] = {a.x, a.y, a.z, a.w};
+      uint32_t c[1];
+      quant_words_f32<FMT, 4>(in, c, s, r);
+      q4[v] = c[0];
+    }
+    for (int64_t i = head + nv * 4 + tid; i < n; i += nthreads)
+      q[i] = quant_one<FMT>(load_f<DT>(x, i), s, r, fin);
   }
 }
 
@@ -536,6 +707,18 @@ static cudaError_t quant_1x128_t(const void* x, int64_t R, int64_t C, uint8_t* q
       return cudaGetLastError();
     }
   } else {
+    if ((xa & 31u) == 0 && (qa & 15u) == 0) {
+      auto k = quant_1x128_f32_v8<FMT>;
+      // 64 CTAs per SM, several waves, as for the 16-bit kernel; each pass of
+      // a CTA moves 32 tiles
+      int64_t grid = (int64_t)sm_count() * 64;
+      const int64_t need = (n_tiles + 4 * (kQuantThreads / 32) - 1) / (4 * (kQuantThreads / 32));
+      if (grid > need) grid = need;
+      if (grid < 1) grid = 1;
+      k<<<(unsigned)grid, kQuantThreads, 0, st>>>(reinterpret_cast<const uint8_t*>(x), n_tiles, q,
+                                                  scales);
+      return cudaGetLastError();
+    }
     if ((xa & 15u) == 0 && (qa & 3u) == 0) {
       auto k = quant_1x128_v32<FMT>;
       const int64_t grid = persistent_grid(k, kQuantThreads / 32, n_tiles);
@@ -590,9 +773,28 @@ static cudaError_t quant_128x128_v8_t(const void* x, int64_t R, int64_t C, uint8
   return cudaGetLastError();
 }
 
+template <int FMT>
+static cudaError_t quant_128x128_f32_v8_t(const void* x, int64_t R, int64_t C, uint8_t* q,
+                                          float* scales, cudaStream_t st) {
+  auto k = quant_128x128_f32_v8<FMT>;
+  int occ = 0;
+  const cudaError_t e = kernel_blocks_per_sm((const void*)k, kQ128Threads, 0, &occ);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  const int64_t nbr = R / 128, nbc = C / 128;
+  int64_t grid = (int64_t)sm_count() * occ;
+  if (grid > nbr * nbc) grid = nbr * nbc;
+  k<<<(unsigned)grid, kQ128Threads, 0, st>>>(reinterpret_cast<const uint8_t*>(x), nbr, nbc, q, C,
+                                             scales);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant_128x128_v8(const void* x, int dtype, int64_t R, int64_t C, int fmt,
                                     uint8_t* q, float* scales, cudaStream_t st) {
   if (R == 0 || C == 0) return cudaSuccess;
+  if (dtype == GS_F32)
+    return fmt == GS_E4M3 ? quant_128x128_f32_v8_t<GS_E4M3>(x, R, C, q, scales, st)
+                          : quant_128x128_f32_v8_t<GS_E5M2>(x, R, C, q, scales, st);
   if (fmt == GS_E4M3)
     return dtype == GS_BF16 ? quant_128x128_v8_t<BF16Tag, GS_E4M3>(x, R, C, q, scales, st)
                             : quant_128x128_v8_t<F16Tag, GS_E4M3>(x, R, C, q, scales, st);

@@ -228,7 +228,7 @@ static cudaError_t launch_tma_t(const CUtensorMap& map, int64_t R, int64_t C, ui
 cudaError_t launch_quant_128x128(const void* x, int dtype, int64_t R, int64_t C, int fmt,
                                  uint8_t* q, float* scales, int32_t* status, cudaStream_t st) {
   if (R == 0 || C == 0) return cudaSuccess;
-  if (dtype != GS_F32 && ((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 15u) == 0)
+  if (((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & (dtype == GS_F32 ? 7u : 15u)) == 0)
     return launch_quant_128x128_v8(x, dtype, R, C, fmt, q, scales, st);
   const bool tma_ok = dtype != GS_F32 && ((uintptr_t)x & 15u) == 0 && ((uintptr_t)q & 7u) == 0 &&
                       R < (int64_t(1) << 31) && C < (int64_t(1) << 31) && encode_fn() != nullptr;

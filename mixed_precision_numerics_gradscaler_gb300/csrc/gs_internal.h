@@ -52,8 +52,8 @@ cudaError_t launch_quant_128x128(const void* x, int dtype, int64_t R, int64_t C,
                                  uint8_t* q, float* scales, int32_t* status,
                                  cudaStream_t stream);
 // The 128x128 kernels behind launch_quant_128x128: direct 32-byte loads
-// (16-bit input, x 32-byte and q 16-byte aligned), and one CTA per block for
-// any dtype and alignment.
+// (x 32-byte aligned; q 16-byte aligned for 16-bit input, 8-byte for FP32),
+// and one CTA per block for any dtype and alignment.
 cudaError_t launch_quant_128x128_v8(const void* x, int dtype, int64_t R, int64_t C, int fmt,
                                     uint8_t* q, float* scales, cudaStream_t stream);
 cudaError_t launch_quant_128x128_simple(const void* x, int dtype, int64_t R, int64_t C, int fmt,

@@ -106,4 +106,41 @@ __device__ __forceinline__ void quant_words(const uint32_t* in, uint32_t* out, f
   }
 }
 
+// ---- FP32 inputs ---------------------------------------------------------------
+// Two FP8 codes (low byte from x0) of two fp32 inputs given as bit patterns,
+// for a finite scale: exact_quotient<2> on both lanes, -x by the sign bit.
+template <int FMT>
+__device__ __forceinline__ uint32_t quant_f32_pair_fast(uint32_t x0, uint32_t x1,
+                                                        const PackedScale& ps) {
+  float lo, hi;
+  upk_f32x2(exact_quotient_x2<2>(pk_f32x2(__uint_as_float(x0 ^ 0x80000000u),
+                                          __uint_as_float(x1 ^ 0x80000000u)),
+                                 ps),
+            lo, hi);
+  return cvt_f32x2_fp8x2<FMT>(hi, lo);
+}
+template <int FMT>
+__device__ __noinline__ uint32_t quant_f32_pair_slow(uint32_t x0, uint32_t x1, float s) {
+  return quant_pair<FMT>(__uint_as_float(x1), __uint_as_float(x0), s, 0.0f, false);
+}
+
+// NW fp32 words -> NW / 4 words of four FP8 codes each, in order.
+template <int FMT, int NW>
+__device__ __forceinline__ void quant_words_f32(const uint32_t* in, uint32_t* out, float s,
+                                                float r) {
+  static_assert(NW % 4 == 0, "four fp32 words per code word");
+  if (isfinite(s)) {
+    const PackedScale ps = packed_scale(s, r);
+#pragma unroll
+    for (int j = 0; j < NW / 4; ++j)
+      out[j] = quant_f32_pair_fast<FMT>(in[4 * j], in[4 * j + 1], ps) |
+               (quant_f32_pair_fast<FMT>(in[4 * j + 2], in[4 * j + 3], ps) << 16);
+  } else {
+#pragma unroll
+    for (int j = 0; j < NW / 4; ++j)
+      out[j] = quant_f32_pair_slow<FMT>(in[4 * j], in[4 * j + 1], s) |
+               (quant_f32_pair_slow<FMT>(in[4 * j + 2], in[4 * j + 3], s) << 16);
+  }
+}
+
 }  // namespace gs

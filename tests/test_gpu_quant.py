@@ -390,22 +390,25 @@ def test_block_quant_random_cases(gs, orc):
 
 
 @pytest.mark.parametrize("path", ["direct", "tma"])
-@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 def test_quant_128x128_several_blocks_per_cta(gs, orc, path, dt, fmt):
     """41 x 13 blocks of 128x128: more blocks than either 128x128 kernel
     launches CTAs (three or two per SM), with a column count that does not
     divide the grid, so CTAs walk several blocks and their block coordinates
     wrap rows -- through the direct-load kernel (32-byte aligned input) and
-    the TMA-staged one (input at a 16-byte offset); block (0, 0) holds NaN,
-    +-Inf, zeros and tiny values. Bit for bit against the oracle."""
-    rng = np.random.default_rng(1000 + 100 * (path == "tma") + 10 * (dt == "f16") + (fmt == "e5m2"))
+    the TMA-staged one (input at a 16-byte offset; FP32 input there takes
+    the one-CTA-per-block kernel); block (0, 0) holds NaN, +-Inf, zeros and
+    tiny values. Bit for bit against the oracle."""
+    rng = np.random.default_rng(1000 + 100 * (path == "tma") + 10 * ["bf16", "f16", "f32"].index(dt)
+                                + (fmt == "e5m2"))
     R, C = 128 * 41, 128 * 13
     xh, xd = _host_input(rng, R, C, dt, special=True)
     if path == "tma":
-        big = torch.zeros(R * C + 8, dtype=xd.dtype, device=DEV)
-        big[8:] = xd.reshape(-1)
-        xd = big[8:].view(R, C)
+        off = 16 // xd.element_size()  # 16 bytes
+        big = torch.zeros(R * C + off, dtype=xd.dtype, device=DEV)
+        big[off:] = xd.reshape(-1)
+        xd = big[off:].view(R, C)
         assert xd.data_ptr() % 32 == 16
     else:
         assert xd.data_ptr() % 32 == 0
