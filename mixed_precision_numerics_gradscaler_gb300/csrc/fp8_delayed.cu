@@ -94,6 +94,54 @@ __global__ void __launch_bounds__(kDelThreads)
   if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }
 
+// FP32 input, x 32-byte and q 8-byte aligned: the same walk over 32-byte
+// vectors of eight elements (two per iteration, a grid apart), eight codes
+// (one 8-byte store) per vector, cast through quant_words_f32.
+template <int FMT>
+__global__ void __launch_bounds__(kDelThreads)
+    quant_delayed_f32_v8(const uint8_t* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
+                         const float* __restrict__ history, int hist_len, float* scale_used,
+                         uint32_t* __restrict__ partials) {
+  __shared__ uint32_t red[kDelThreads / 32];
+  const float s = block_scale<FMT>(__uint_as_float(history_max_bits(history, hist_len, red)));
+  const bool fin = isfinite(s);
+  const float r = __frcp_rn(s);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_used = s;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t nv = n >> 3;  // 8 elements (32 bytes) per vector
+  const uint32_t mm = 0x7FFFFFFFu;
+  uint32_t m = 0;
+  int64_t v = tid;
+  for (; v + nthreads < nv; v += 2 * nthreads) {
+    const V8 a = ld_stream8(x + 32 * v), b = ld_stream8(x + 32 * (v + nthreads));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, max(a.w[j] & mm, b.w[j] & mm));
+    uint32_t ca[2], cb[2];
+    quant_words_f32<FMT, 8>(a.w, ca, s, r);
+    quant_words_f32<FMT, 8>(b.w, cb, s, r);
+    st_stream(reinterpret_cast<uint2*>(q + 8 * v), make_uint2(ca[0], ca[1]));
+    st_stream(reinterpret_cast<uint2*>(q + 8 * (v + nthreads)), make_uint2(cb[0], cb[1]));
+  }
+  for (; v < nv; v += nthreads) {
+    const V8 a = ld_stream8(x + 32 * v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, a.w[j] & mm);
+    uint32_t ca[2];
+    quant_words_f32<FMT, 8>(a.w, ca, s, r);
+    st_stream(reinterpret_cast<uint2*>(q + 8 * v), make_uint2(ca[0], ca[1]));
+  }
+  // ragged tail (n not a multiple of 8)
+  const float* xf = reinterpret_cast<const float*>(x);
+  for (int64_t i = nv * 8 + tid; i < n; i += nthreads) {
+    const float f = xf[i];
+    m = max(m, __float_as_uint(f) & mm);
+    q[i] = (uint8_t)(quant_pair<FMT, 2>(0.0f, f, s, r, fin) & 0xFFu);
+  }
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
 // Any dtype and alignment, element by element.
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kDelThreads)
@@ -154,13 +202,17 @@ static cudaError_t delayed_t(const void* x, int64_t n, uint8_t* q, float* histor
   // persistent wave) and at most kMaxAmaxBlocks partials.
   bool vec = false;
   if constexpr (DT != GS_F32) vec = ((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 15u) == 0;
+  else vec = ((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 7u) == 0;
   using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
   int64_t grid = (n + kDelThreads * 32 - 1) / (kDelThreads * 32);
   const int64_t cap = (int64_t)sm_count() * 16;
   if (grid > cap) grid = cap;
   if (grid > kMaxAmaxBlocks) grid = kMaxAmaxBlocks;
   if (grid < 1) grid = 1;
-  if (vec)
+  if (vec && DT == GS_F32)
+    quant_delayed_f32_v8<FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(
+        reinterpret_cast<const uint8_t*>(x), n, q, history, hist_len, scale_used, partials);
+  else if (vec)
     quant_delayed_v8<Tag, FMT><<<(unsigned)grid, kDelThreads, 0, st>>>(
         reinterpret_cast<const uint8_t*>(x), n, q, history, hist_len, scale_used, partials);
   else

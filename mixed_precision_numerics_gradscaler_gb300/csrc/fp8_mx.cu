@@ -9,7 +9,8 @@
 // the product leaves the normal range), so x * 2^-e is the IEEE quotient
 // x / 2^e.
 //
-// Layout: one lane per 32-element block -- two 32-byte loads (16-bit input),
+// Layout: one lane per 32-element block -- two 32-byte loads (16-bit input;
+// FP32 input takes two lanes per block, quant_mx_f32_v8),
 // amax on magnitude bit patterns, the exponent read from the amax's fp32
 // exponent field, one 32-byte store of 32 codes and one scale byte (a warp
 // writes 32 consecutive scale bytes).  HBM-bound: 2 + 1 + 1/32 bytes per
@@ -18,6 +19,7 @@
 #include <stdint.h>
 
 #include "gs_device.cuh"
+#include "gs_quant.cuh"
 #include "gs_internal.h"
 
 namespace gs {
@@ -100,6 +102,66 @@ __global__ void __launch_bounds__(kMxThreads)
     }
     st_stream8(q + b * 32, o);
     scales[b] = (uint8_t)code;
+  }
+}
+
+// FP32 input, x 32-byte and q 16-byte aligned: two lanes per 32-element
+// block, each with two adjacent 32-byte loads (16 elements); the pair's amax
+// by one shuffle; each lane writes 16 codes with one 16-byte store and the
+// even lane the scale byte.  Elements scale by the exact power of two on
+// f32x2 pairs (each lane an IEEE fp32 multiply).
+template <int FMT>
+__global__ void __launch_bounds__(kMxThreads)
+    quant_mx_f32_v8(const uint8_t* __restrict__ x, int64_t n_blocks, uint8_t* __restrict__ q,
+                    uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t n_halves = 2 * n_blocks;
+  // warp-uniform loop bound: both lanes of a pair always reach the shuffle
+  for (int64_t base = warp * 32; base < n_halves; base += n_warps * 32) {
+    const int64_t h = base + lane, b = h >> 1;
+    const int part = lane & 1;
+    const bool live = h < n_halves;  // false for both lanes of a pair together
+    V8 a, c;
+    if (live) {
+      a = ld_stream8(x + b * 128 + part * 64);
+      c = ld_stream8(x + b * 128 + part * 64 + 32);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a.w[j] = c.w[j] = 0;
+    }
+    const uint32_t mm = 0x7FFFFFFFu;
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, max(a.w[j] & mm, c.w[j] & mm));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    uint32_t o[4];
+    int code;
+    if (m >= 0x7F800000u) {  // Inf or NaN in the block
+      code = 255;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = 0x7F7F7F7Fu;
+    } else {
+      code = mx_code<FMT>(m);
+      const float k = mx_inv_scale(code);
+      const uint64_t k2 = pk_f32x2(k, k);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const V8& v = j < 2 ? a : c;
+        const int w0 = 4 * (j & 1);
+        float l0, h0, l1, h1;
+        upk_f32x2(mul_f32x2(pk_f32x2(__uint_as_float(v.w[w0]), __uint_as_float(v.w[w0 + 1])), k2),
+                  l0, h0);
+        upk_f32x2(mul_f32x2(pk_f32x2(__uint_as_float(v.w[w0 + 2]), __uint_as_float(v.w[w0 + 3])), k2),
+                  l1, h1);
+        o[j] = cvt_f32x2_fp8x2<FMT>(h0, l0) | (cvt_f32x2_fp8x2<FMT>(h1, l1) << 16);
+      }
+    }
+    if (live) {
+      *reinterpret_cast<uint4*>(q + b * 32 + part * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+      if (part == 0) scales[b] = (uint8_t)code;
+    }
   }
 }
 
@@ -197,6 +259,9 @@ static cudaError_t quant_mx_t(const void* x, int64_t nb, uint8_t* q, uint8_t* s,
   if (DT != GS_F32 && ((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 31u) == 0) {
     using Tag = typename std::conditional<DT == GS_BF16, BF16Tag, F16Tag>::type;
     quant_mx_v8<Tag, FMT><<<(unsigned)mx_grid(nb), kMxThreads, 0, st>>>(
+        reinterpret_cast<const uint8_t*>(x), nb, q, s);
+  } else if (DT == GS_F32 && ((uintptr_t)x & 31u) == 0 && ((uintptr_t)q & 15u) == 0) {
+    quant_mx_f32_v8<FMT><<<(unsigned)mx_grid(2 * nb), kMxThreads, 0, st>>>(
         reinterpret_cast<const uint8_t*>(x), nb, q, s);
   } else {
     quant_mx_any<DT, FMT><<<(unsigned)mx_grid(nb), kMxThreads, 0, st>>>(x, nb, q, s);
