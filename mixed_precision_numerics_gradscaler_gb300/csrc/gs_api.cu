@@ -202,8 +202,8 @@ int gs_tensor_list_create(const void* const* grads, void* const* outs, const int
       read.push_back(Span{(uintptr_t)grads[i], (uintptr_t)grads[i] + (uintptr_t)n * 2});
       const uint16_t* g = static_cast<const uint16_t*>(grads[i]);
       float* o = static_cast<float*>(outs[i]);
-      for (int64_t off = 0; off < n; off += kChunkElems)
-        chunks.push_back(Chunk{g + off, o + off, (n - off) < kChunkElems ? (n - off) : kChunkElems});
+      const int64_t head = chunk_head(g, o, n), nc = chunk_count(n, head);
+      for (int64_t c = 0; c < nc; ++c) chunks.push_back(chunk_at(g, o, n, head, c));
       total += n;
     }
     // one launch covers every tensor: no output may overlap any input or

@@ -51,12 +51,10 @@ __global__ void noalloc_build_chunks(const __grid_constant__ TensorTable tt, uns
     ws->found = 0;
   }
   for (int t = 0; t < tt.n; ++t) {
-    const int64_t n = tt.numel[t], nc = (n + kChunkElems - 1) / kChunkElems;
-    for (int64_t c = threadIdx.x; c < nc; c += blockDim.x) {
-      const int64_t off = c * kChunkElems;
-      chunks[tt.first_chunk[t] + c] =
-          Chunk{tt.in[t] + off, tt.out[t] + off, (n - off) < kChunkElems ? (n - off) : kChunkElems};
-    }
+    const int64_t n = tt.numel[t], head = chunk_head(tt.in[t], tt.out[t], n);
+    const int64_t nc = chunk_count(n, head);
+    for (int64_t c = threadIdx.x; c < nc; c += blockDim.x)
+      chunks[tt.first_chunk[t] + c] = chunk_at(tt.in[t], tt.out[t], n, head, c);
   }
 }
 
@@ -115,9 +113,10 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
     const int64_t n = numels[i];
     if (n < 0 || n > (INT64_MAX >> 3)) return GS_ERR_SHAPE;
     if (n == 0) continue;
-    const int64_t nc = (n + kChunkElems - 1) / kChunkElems;
-    if (nc > kNoAllocMaxChunks - n_chunks) return GS_ERR_SHAPE;  // beyond the scratch array
     if (!grads[i] || !outs[i]) return GS_ERR_NULL;
+    const int64_t nc = chunk_count(n, chunk_head(static_cast<const uint16_t*>(grads[i]),
+                                                 static_cast<const float*>(outs[i]), n));
+    if (nc > kNoAllocMaxChunks - n_chunks) return GS_ERR_SHAPE;  // beyond the scratch array
     tt.in[tt.n] = static_cast<const uint16_t*>(grads[i]);
     tt.out[tt.n] = static_cast<float*>(outs[i]);
     tt.numel[tt.n] = n;

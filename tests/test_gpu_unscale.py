@@ -338,3 +338,43 @@ def test_random_lists_views_and_scales(gs, orc):
             outs.append(bo[go:go + h.size])
         S = float(2.0 ** int(rng.integers(-20, 30))) if rng.integers(0, 2) else float(rng.uniform(0.1, 1e6))
         _run_list(gs, orc, hosts, S, views=(grads, outs))
+
+
+def _chunk_head(in_addr, out_addr, n):
+    """Elements before the first element where both the FP16 input and the
+    FP32 output are 32-byte aligned (0: none before the end, or aligned)."""
+    h = ((32 - in_addr % 32) % 32) // 2
+    if h == 0 or h >= n:
+        return 0
+    return h if (out_addr + 4 * h) % 32 == 0 else 0
+
+
+def test_flat_buffer_list_at_every_offset(gs, orc):
+    """Tensors packed back to back in one flat FP16 buffer and one flat FP32
+    buffer (so most start off 32-byte alignment, as in a flat gradient
+    bucket): the list starts each tensor's full chunks where input and
+    output are aligned, after one short head chunk. Outputs, found_inf and
+    scaler state bit for bit against the oracle; the chunk count matches
+    that split; one NaN in the last tensor is found."""
+    rng = np.random.default_rng(2024)
+    sizes = [1, 15, 16, 17, 31, 8191, 8192, 8193, 16401, 70001, 30, 3, 12345]
+    hosts = [(rng.standard_normal(n) * 40).astype(np.float16).view(np.uint16) for n in sizes]
+    hosts[-1][777] = 0x7E00
+    total = sum(sizes) + 7
+    fin = torch.zeros(total, dtype=torch.float16, device=DEV)
+    fout = torch.full((total,), 7.0, dtype=torch.float32, device=DEV)
+    grads, outs, off, want_chunks = [], [], 1, 0
+    for h in hosts:
+        n = h.size
+        g, o = fin[off:off + n], fout[off:off + n]
+        g.copy_(to_dev16(h, torch.float16))
+        head = _chunk_head(g.data_ptr(), o.data_ptr(), n)
+        want_chunks += (1 if head else 0) + (n - head + 8191) // 8192
+        grads.append(g)
+        outs.append(o)
+        off += n
+    tl = gs.gs_tensor_list_create(grads, outs)
+    assert tl.info()[1] == want_chunks
+    tl.close()
+    assert _run_list(gs, orc, hosts, 2.0 ** 12, views=(grads, outs)) == 1
+    assert (fout[:1] == 7.0).all() and (fout[off:] == 7.0).all()

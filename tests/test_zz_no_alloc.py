@@ -102,3 +102,34 @@ def test_noalloc_rejects_outputs_that_alias_another_tensor(gs):
     gs.gs_unscale_check_update_noalloc(g, [buf[:n], buf[n:]], scale, tracker, found, skipped)
     torch.cuda.synchronize()
     assert tracker.item() == 1
+
+
+def test_noalloc_flat_buffer_equals_list(gs):
+    """Tensors packed back to back in flat FP16 / FP32 buffers (most start
+    off 32-byte alignment, so each gets a short head chunk): the
+    allocation-free step gives the list step's outputs and state."""
+    rng = np.random.default_rng(77)
+    sizes = [1, 15, 17, 8191, 8193, 16401, 70001, 30, 12345]
+    total = sum(sizes) + 5
+    fin = torch.from_numpy((rng.standard_normal(total) * 40).astype(np.float16)).to(DEV)
+    fin[total - 100] = float("inf")
+    runs = []
+    for use_list in (True, False):
+        fout = torch.full((total,), 7.0, dtype=torch.float32, device=DEV)
+        grads, outs, off = [], [], 3
+        for n in sizes:
+            grads.append(fin[off:off + n])
+            outs.append(fout[off:off + n])
+            off += n
+        state = _state(4096.0)
+        if use_list:
+            tl = gs.gs_tensor_list_create(grads, outs)
+            gs.gs_unscale_check_update(tl, *state, 2.0, 0.5, 5)
+        else:
+            gs.gs_unscale_check_update_noalloc(grads, outs, *state, 2.0, 0.5, 5)
+        torch.cuda.synchronize()
+        if use_list:
+            tl.close()
+        runs.append((fout.view(torch.int32).clone(), [t.item() for t in state]))
+    assert torch.equal(runs[0][0], runs[1][0])
+    assert runs[0][1] == runs[1][1]
