@@ -326,7 +326,11 @@ int gs_param_list_create(float* const* master, uint16_t* const* master_bf16,
       written.push_back(Span{(uintptr_t)master[i], (uintptr_t)master[i] + (uintptr_t)n * 4});
       if (wb) written.push_back(Span{(uintptr_t)wb, (uintptr_t)wb + (uintptr_t)n * 2});
       read.push_back(Span{(uintptr_t)grads[i], (uintptr_t)grads[i] + (uintptr_t)n * 4});
-      for (int64_t off = 0; off < n; off += kChunkElems)
+      // a short head chunk up to the first element where the vector path's
+      // alignments hold, then full chunks from there
+      const int64_t head = mchunk_head(master[i], wb, grads[i], n);
+      if (head > 0) chunks.push_back(MChunk{master[i], wb, grads[i], head});
+      for (int64_t off = head; off < n; off += kChunkElems)
         chunks.push_back(MChunk{master[i] + off, wb ? wb + off : nullptr, grads[i] + off,
                                 (n - off) < kChunkElems ? (n - off) : kChunkElems});
       total += n;

@@ -71,6 +71,20 @@ struct MChunk {
   int64_t n;
 };
 
+// The same split for a parameter tensor: elements before the first element
+// at which the fp32 master and gradient are 32-byte aligned and the bf16
+// copy (if any) 16-byte aligned -- the master update's vector path -- or 0
+// when there is no such element before the end (or the tensor starts
+// aligned).
+__host__ __device__ inline int64_t mchunk_head(const float* w, const uint16_t* wb,
+                                               const float* g, int64_t n) {
+  const int64_t h = (int64_t)(((32u - ((uint32_t)(uintptr_t)w & 31u)) & 31u) >> 2);
+  if (h == 0 || h >= n) return 0;
+  if ((((uintptr_t)(g + h)) & 31u) != 0) return 0;
+  if (wb && (((uintptr_t)(wb + h)) & 15u) != 0) return 0;
+  return h;
+}
+
 // Loss-scale policy applied by the last CTA of the unscale kernel.  With
 // hyst == nullptr it is the GradScaler loop; otherwise the hysteresis
 // policy: an overflow spends one unit of *hyst (S kept) until one is left,

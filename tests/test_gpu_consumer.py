@@ -173,3 +173,38 @@ def test_master_update_random_lists(gs, orc):
             if with_bf16 and found_v:
                 assert (bits_of(wb[i]) == 0).all()           # a skipped step writes nothing
         pl.close()
+
+
+def test_master_update_flat_buffers_at_every_offset(gs, orc):
+    """Master weights, gradients and bf16 copies packed back to back in three
+    flat buffers, so most tensors start off the vector path's alignment:
+    each gets a short head chunk and then aligned chunks. The update against
+    the oracle, bit for bit, and nothing outside the tensors written."""
+    rng = np.random.default_rng(919)
+    sizes = [1, 7, 8, 9, 8191, 8192, 8200, 30011, 5]
+    total = sum(sizes) + 3
+    w_flat_h = (rng.standard_normal(total) * 0.02).astype(np.float32)
+    g_flat_h = (rng.standard_normal(total) * 1e-2).astype(np.float32)
+    W = torch.from_numpy(w_flat_h.copy()).to(DEV)
+    G = torch.from_numpy(g_flat_h).to(DEV)
+    B = torch.zeros(total, dtype=torch.bfloat16, device=DEV)
+    w, g, wb, spans, off = [], [], [], [], 3
+    for n in sizes:
+        w.append(W[off:off + n])
+        g.append(G[off:off + n])
+        wb.append(B[off:off + n])
+        spans.append((off, n))
+        off += n
+    norm = torch.tensor([1.0], dtype=torch.float32, device=DEV)
+    found = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pl = gs.gs_param_list_create(w, g, wb)
+    gs.gs_master_update_sgd(pl, 0.1, 0.0, norm, found)
+    torch.cuda.synchronize()
+    pl.close()
+    w_out, b_out = W.cpu().numpy(), bits_of(B)
+    for i, (o, n) in enumerate(spans):
+        ref_w = w_flat_h[o:o + n].copy()
+        ref_b = orc.master_update_sgd(ref_w, g_flat_h[o:o + n], 0.1, 1.0, 0)
+        assert_same_f32(w_out[o:o + n], ref_w, f"tensor {i}")
+        assert same_bf16(b_out[o:o + n], ref_b).all(), f"tensor {i} bf16"
+    assert (w_out[:3] == w_flat_h[:3]).all() and (b_out[:3] == 0).all()
