@@ -394,7 +394,7 @@ def test_block_quant_random_cases(gs, orc):
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 def test_quant_128x128_several_blocks_per_cta(gs, orc, path, dt, fmt):
     """41 x 13 blocks of 128x128: more blocks than either 128x128 kernel
-    launches CTAs (three or two per SM), with a column count that does not
+    launches CTAs (two per SM), with a column count that does not
     divide the grid, so CTAs walk several blocks and their block coordinates
     wrap rows -- through the direct-load kernel (32-byte aligned input) and
     the TMA-staged one (input at a 16-byte offset; FP32 input there takes
