@@ -312,6 +312,68 @@ def test_cfg4_grad_e5m2_per_tensor_full_size(gs, orc):
     assert_same_bytes(got, want, "cfg4 grad codes")
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("x_off,q_off", [(0, 0), (1, 0), (0, 3), (8, 8)])
+def test_quant_tensor_runs_and_offsets(gs, orc, fmt, dt, x_off, q_off):
+    """Pass 2 of the per-tensor quantiser walks its vector body from the end
+    in runs of two 1024-vector iterations per CTA: sizes below one
+    iteration, at a run boundary, and several runs with a partial last
+    iteration, with the input and the codes at element offsets that move
+    the scalar head and tail (or send everything to the scalar path).  Bit
+    for bit against the oracle; the bytes around the codes stay untouched."""
+    vec = 4 if dt == "f32" else 8
+    rng = np.random.default_rng(x_off * 31 + q_off * 7 + vec + (fmt == "e5m2"))
+    for n in (vec * 1024 - 3, 2 * 2 * vec * 1024, 5 * 2 * vec * 1024 + 517 * vec + 5):
+        xh, xd = _host_input(rng, 1, n + x_off, dt, special=bool(rng.integers(0, 2)))
+        xh = np.ascontiguousarray(xh.reshape(-1)[x_off:])
+        xd = xd.reshape(-1)[x_off:]
+        qbase = torch.full((n + 16,), 0xAB, dtype=torch.uint8, device=DEV)
+        q = qbase[q_off:q_off + n]
+        s = torch.empty(1, dtype=torch.float32, device=DEV)
+        ws = torch.full((gs.gs_ws_bytes() // 4,), -1, dtype=torch.int32, device=DEV)
+        gs.fp8_quant_tensor(xd, fmt, q, s, ws)
+        rq, rs = orc.quant_tensor(xh, FMT[fmt], dtype=ODT[dt])
+        torch.cuda.synchronize()
+        assert_same_bytes(q.cpu().numpy(), rq, f"per-tensor codes n={n}")
+        assert_same_f32(s.cpu().numpy(), rs, f"per-tensor scale n={n}")
+        assert (qbase[:q_off] == 0xAB).all() and (qbase[q_off + n:] == 0xAB).all()
+
+
+def test_quant_tensor_grid_cap_sampled(gs, orc):
+    """A bf16 tensor long enough that pass 2 has more runs than its grid
+    (128 CTAs per SM), so CTAs take a second run further down the tensor:
+    the oracle's amax over the whole host-regenerated tensor gives the
+    scale; codes are compared on contiguous slabs (both ends, the runs
+    where the grid wraps) and 100k random positions."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    run = 2 * 1024 * 8                      # elements per run
+    n = sms * 128 * run + 3000 * run + 12345
+    g = wl.cfg4_grad()
+    st = torch.cuda.current_stream().cuda_stream
+    x = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    dg.fill_device(g.spec, 0, n, x.data_ptr(), st)
+    q = torch.empty(n, dtype=torch.uint8, device=DEV)
+    s = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=DEV)
+    gs.fp8_quant_tensor(x, "e5m2", q, s, ws)
+    xh = dg.fill_host(g.spec, 0, n)
+    rs = orc.scale_from_amax(orc.amax(xh, dtype=1), 1)
+    torch.cuda.synchronize()
+    assert s.item() == rs
+    del x
+    # runs are counted from the end: the runs past the grid (each CTA's
+    # second) begin within one run of this element
+    wrap = n - 12345 - sms * 128 * run
+    rng = np.random.default_rng(11)
+    slabs = [np.arange(0, 20000), np.arange(n - 20000, n), np.arange(wrap - 20000, wrap + 20000),
+             rng.integers(0, n, 100000)]
+    idx = np.unique(np.concatenate(slabs)).astype(np.int64)
+    want = np.array([orc.quant_one(float(v), rs, 1) for v in orc.decode_array(xh[idx], 1)], np.uint8)
+    got = q[torch.from_numpy(idx).to(DEV)].cpu().numpy()
+    assert_same_bytes(got, want, "per-tensor codes past the grid cap")
+
+
 def test_quant_deterministic(gs):
     a = wl.cfg1_act()
     x = to_dev16(dg.fill_host(a.spec, 0, a.numel), torch.bfloat16).view(a.rows, a.cols)
