@@ -48,7 +48,8 @@ def _steps(rng, n, dt):
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
-@pytest.mark.parametrize("n,x_off", [(100003, 0), (4096, 0), (31, 0), (70001, 1), (65536, 8)])
+@pytest.mark.parametrize("n,x_off", [(100003, 0), (4096, 0), (31, 0), (70001, 1), (65536, 8),
+                                      (9 * 2 ** 20 + 37, 0)])
 def test_delayed_scaling_steps(gs, orc, fmt, dt, n, x_off):
     H = 3
     rng = np.random.default_rng(n + x_off)
