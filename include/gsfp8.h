@@ -18,8 +18,9 @@
  *     legacy default stream.  Every compute call is asynchronous on that
  *     stream and never synchronises the host.
  *   - Memory: every data pointer is device memory of the current device
- *     (or managed / mapped host memory the device can reach); pointers the
- *     device cannot reach are rejected with GS_ERR_ARG.  The caller owns all
+ *     (or managed memory, or mapped host memory whose device address equals
+ *     its host address); pointers the device cannot use as given are
+ *     rejected with GS_ERR_ARG.  The caller owns all
  *     data buffers.  The library allocates only inside
  *     gs_tensor_list_create; no compute call allocates.
  *   - Layout: row-major and contiguous; element [r, c] of an R x C array is

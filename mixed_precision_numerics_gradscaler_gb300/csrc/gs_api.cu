@@ -103,8 +103,10 @@ static int cuda_fail(cudaError_t e) {
   return GS_ERR_CUDA;
 }
 
-// A pointer the current device can dereference: device memory of this
-// device, managed memory, or mapped (registered) host memory.
+// A pointer the current device can dereference as it is: device memory of
+// this device, managed memory, or mapped (registered) host memory whose
+// device address is the host address itself (the kernels are given p, not
+// a translated alias).
 static bool device_reachable(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -117,7 +119,7 @@ static bool device_reachable(const void* p) {
     case cudaMemoryTypeManaged:
       return true;
     case cudaMemoryTypeHost:
-      return a.devicePointer != nullptr;
+      return a.devicePointer == p;
     default:
       return false;
   }

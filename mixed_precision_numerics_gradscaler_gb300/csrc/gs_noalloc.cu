@@ -141,9 +141,10 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
       return GS_ERR_ARG;
     }
     for (const cudaPointerAttributes* p : {&pa, &pb}) {
+      const void* given = (p == &pa) ? (const void*)tt.in[i] : (const void*)tt.out[i];
       const bool ok = (p->type == cudaMemoryTypeDevice && p->device == current_device()) ||
                       p->type == cudaMemoryTypeManaged ||
-                      (p->type == cudaMemoryTypeHost && p->devicePointer != nullptr);
+                      (p->type == cudaMemoryTypeHost && p->devicePointer == given);
       if (!ok) return GS_ERR_ARG;
     }
   }
@@ -162,7 +163,7 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
     }
     const bool ok = (a.type == cudaMemoryTypeDevice && a.device == current_device()) ||
                     a.type == cudaMemoryTypeManaged ||
-                    (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+                    (a.type == cudaMemoryTypeHost && a.devicePointer == p);
     if (!ok) return GS_ERR_ARG;
   }
   cudaError_t e = cudaSuccess;

@@ -378,3 +378,41 @@ def test_flat_buffer_list_at_every_offset(gs, orc):
     tl.close()
     assert _run_list(gs, orc, hosts, 2.0 ** 12, views=(grads, outs)) == 1
     assert (fout[:1] == 7.0).all() and (fout[off:] == 7.0).all()
+
+
+def test_scaler_state_in_host_memory(gs, orc):
+    """S, the growth tracker and found_inf kept in pinned host memory (mapped:
+    its device address is its host address) are read and updated by the
+    kernel like device memory, three steps against the oracle (the second
+    overflows); the same state in pageable host memory is rejected with
+    GS_ERR_ARG before anything is launched, and the state is left as it was."""
+    rng = np.random.default_rng(77)
+    hosts = [(rng.standard_normal(n) * 100).astype(np.float16).view(np.uint16) for n in (5000, 12345)]
+    grads = [to_dev16(h, torch.float16) for h in hosts]
+    outs = [torch.empty(h.size, dtype=torch.float32, device=DEV) for h in hosts]
+    tl = gs.gs_tensor_list_create(grads, outs)
+    scale = torch.tensor([1024.0], dtype=torch.float32).pin_memory()
+    tracker = torch.zeros(1, dtype=torch.int32).pin_memory()
+    found = torch.zeros(1, dtype=torch.int32).pin_memory()
+    ref = orc.ScalerState(1024.0, 0)
+    for step in range(3):
+        hs = [h.copy() for h in hosts]
+        if step == 1:
+            hs[1][4321] = 0x7C00  # +Inf
+            grads[1][4321] = float("inf")
+        elif step == 2:
+            grads[1].copy_(to_dev16(hosts[1], torch.float16))
+        gs.gs_unscale_check_update(tl, scale, tracker, found, None, 2.0, 0.5, 2)
+        ref_outs, ref_found = ref.step(hs, 2.0, 0.5, 2)
+        torch.cuda.synchronize()
+        for o, r in zip(outs, ref_outs):
+            assert_same_f32(o.cpu().numpy(), r, f"step {step}")
+        assert int(found[0]) == ref_found == (1 if step == 1 else 0)
+        assert float(scale[0]) == ref.scale.value
+        assert int(tracker[0]) == ref.growth_tracker.value
+    pageable = [torch.tensor([1024.0]), torch.zeros(1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32)]
+    with pytest.raises(gs.GsError) as ei:
+        gs.gs_unscale_check_update(tl, *pageable, None, 2.0, 0.5, 2)
+    assert ei.value.status == gs.GS_ERR_ARG
+    assert float(pageable[0][0]) == 1024.0 and int(pageable[1][0]) == 0
+    tl.close()
