@@ -101,6 +101,53 @@ def throughput(total_bytes: float, elapsed_s: float) -> float:
     return total_bytes / elapsed_s / 1e9
 
 
+def link_ceiling(step_bytes: float, h2d_bytes: float, d2h_bytes: float, h2d_gbs: float,
+                 d2h_gbs: float, both_gbs: float) -> float:
+    """Best end-to-end rate the host link allows, in the metric's unit
+    (algorithmic bytes of one step / the shortest time its copies can take):
+    both directions share the link (each at half the measured concurrent
+    total) until the smaller transfer is done, then the rest of the larger
+    one runs alone at its own one-way rate."""
+    each = both_gbs / 2.0
+    common = min(h2d_bytes, d2h_bytes)
+    rest, rest_gbs = (d2h_bytes - common, d2h_gbs) if d2h_bytes >= h2d_bytes else \
+        (h2d_bytes - common, h2d_gbs)
+    t = common / (each * 1e9) + rest / (rest_gbs * 1e9)
+    return step_bytes / t / 1e9 if t > 0 else 0.0
+
+
+def measure_link(torch, nbytes: int = 1 << 30, reps: int = 3) -> dict:
+    """Pinned host <-> device copy rates on this machine (best of `reps`): one
+    way each, and both at once on two streams."""
+    d1 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    h1 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best(fn, moved):
+        ms = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ms.append(time.perf_counter() - t0)
+        return moved / min(ms) / 1e9
+
+    def both():
+        with torch.cuda.stream(s1):
+            d1.copy_(h1, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    r = {"h2d_gbs": round(best(lambda: d1.copy_(h1, non_blocking=True), nbytes), 1),
+         "d2h_gbs": round(best(lambda: h2.copy_(d2, non_blocking=True), nbytes), 1),
+         "both_gbs": round(best(both, 2 * nbytes), 1)}
+    del d1, d2, h1, h2
+    return r
+
+
 # ---- peaks, traffic, clocks --------------------------------------------------------
 
 def fp8_peak(timed_s: float) -> tuple[float, str]:
@@ -588,7 +635,12 @@ def run_ours(args):
         if dist:
             dist.barrier()
         max_e2e, tot = aggregate(el, float(w.bytes_per_step * args.e2e_steps), dist, dev)
+        link = measure_link(torch)
+        link["ceiling_gbs"] = round(link_ceiling(w.bytes_per_step, w.h2d_bytes, w.d2h_bytes,
+                                                 link["h2d_gbs"], link["d2h_gbs"],
+                                                 link["both_gbs"]), 1)
         e2e = {"value": throughput(tot, max_e2e), "unit": UNIT,
+               "link": link,
                "h2d_bytes_per_step": w.h2d_bytes, "d2h_bytes_per_step": w.d2h_bytes,
                "steps": args.e2e_steps, "ms_per_step": 1000 * max_e2e / args.e2e_steps,
                "pipeline": "two device buffer sets; step k+1's upload and step k-1's download "

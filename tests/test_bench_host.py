@@ -1,8 +1,10 @@
 """Host-side pieces of bench.py on CPU: the clock-record parser, the choice
-of FP8 peak, the staleness rule of the recorded DRAM traffic, and the
-threaded oracle runner."""
+of FP8 peak, the staleness rule of the recorded DRAM traffic, the
+threaded oracle runner, and the host-link ceiling of the end-to-end leg."""
 import json
 import threading
+
+import pytest
 
 import bench
 
@@ -96,3 +98,18 @@ def test_reference_arm_prints_one_complete_line(monkeypatch, capsys):
     assert cb["sample"] and cb["cpu_model"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_link_ceiling_two_phase():
+    """Both directions share the link at half its concurrent rate until the
+    smaller transfer ends; the rest of the larger one runs at its one-way
+    rate; the result is the step's bytes over that time."""
+    import bench
+    # 10 GB up and 20 GB down, 50 GB/s each while both run, then 10 GB down
+    # alone at 50 GB/s: 0.2 s + 0.2 s for a 30 GB step
+    assert bench.link_ceiling(30e9, 10e9, 20e9, 100.0, 50.0, 100.0) == pytest.approx(75.0)
+    # the upload is the larger one: its rest runs at the upload rate
+    # (0.2 s shared + 10 GB at 25 GB/s = 0.6 s)
+    assert bench.link_ceiling(30e9, 20e9, 10e9, 25.0, 400.0, 100.0) == pytest.approx(50.0)
+    # equal transfers never leave the shared phase
+    assert bench.link_ceiling(2e9, 1e9, 1e9, 999.0, 999.0, 100.0) == pytest.approx(100.0)
