@@ -208,3 +208,31 @@ def test_master_update_flat_buffers_at_every_offset(gs, orc):
         assert_same_f32(w_out[o:o + n], ref_w, f"tensor {i}")
         assert same_bf16(b_out[o:o + n], ref_b).all(), f"tensor {i} bf16"
     assert (w_out[:3] == w_flat_h[:3]).all() and (b_out[:3] == 0).all()
+
+
+def test_norm_one_llama_layer(gs, orc):
+    """The fused norm over the first layer of the Llama-3-8B-shaped list
+    (9 tensors, 218 M elements: more chunks than the grid has CTAs, so CTAs
+    add several chunk sums and every slot of the last-CTA reduction is
+    used), against the oracle's compensated sum over host-regenerated
+    inputs; outputs and state equal the plain step's."""
+    cfg = wl.cfg2_grads()
+    n_t = 9
+    st = torch.cuda.current_stream().cuda_stream
+    grads = [torch.empty(n, dtype=torch.float16, device=DEV) for n in cfg.numels[:n_t]]
+    for t, g in enumerate(grads):
+        dg.fill_device(cfg.spec(t, 0), 0, g.numel(), g.data_ptr(), st)
+    outs = [torch.empty(n, dtype=torch.float32, device=DEV) for n in cfg.numels[:n_t]]
+    tl = gs.gs_tensor_list_create(grads, outs)
+    assert tl.info()[1] > torch.cuda.get_device_properties(0).multi_processor_count * 128
+    s = _state()
+    norm = torch.empty(1, dtype=torch.float32, device=DEV)
+    gs.gs_unscale_check_update_norm(tl, *s, norm, None, 2.0, 0.5, 2000)
+    hosts = [dg.fill_host(cfg.spec(t, 0), 0, n) for t, n in enumerate(cfg.numels[:n_t])]
+    ref = orc.ScalerState(2.0 ** 16)
+    ref_outs, ref_found = ref.step(hosts, 2.0, 0.5, 2000)
+    want = orc.grad_norm(ref_outs)
+    torch.cuda.synchronize()
+    assert s[2].item() == ref_found == 0
+    assert abs(norm.item() ** 2 - want ** 2) <= NORM_REL_TOL * want ** 2, (norm.item(), want)
+    tl.close()
