@@ -107,7 +107,7 @@ static int cuda_fail(cudaError_t e) {
 // this device, managed memory, or mapped (registered) host memory whose
 // device address is the host address itself (the kernels are given p, not
 // a translated alias).
-static bool device_reachable(const void* p) {
+bool device_reachable(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();  // clear the sticky-free error of the query

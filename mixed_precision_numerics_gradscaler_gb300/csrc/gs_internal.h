@@ -21,6 +21,9 @@ int current_device();
 
 // Records e as the calling thread's last CUDA error (gs_last_cuda_error).
 void record_cuda_error(cudaError_t e);
+// True if the current device can dereference p as given: its own device
+// memory, managed memory, or mapped host memory whose device address is p.
+bool device_reachable(const void* p);
 
 // A byte range [lo, hi) of memory.
 struct Span {

@@ -134,19 +134,7 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
     const uintptr_t a = (uintptr_t)tt.in[i], b = (uintptr_t)tt.out[i];
     written[i] = Span{b, b + (uintptr_t)n * 4};
     read[i] = Span{a, a + (uintptr_t)n * 2};
-    cudaPointerAttributes pa, pb;
-    if (cudaPointerGetAttributes(&pa, tt.in[i]) != cudaSuccess ||
-        cudaPointerGetAttributes(&pb, tt.out[i]) != cudaSuccess) {
-      cudaGetLastError();
-      return GS_ERR_ARG;
-    }
-    for (const cudaPointerAttributes* p : {&pa, &pb}) {
-      const void* given = (p == &pa) ? (const void*)tt.in[i] : (const void*)tt.out[i];
-      const bool ok = (p->type == cudaMemoryTypeDevice && p->device == current_device()) ||
-                      p->type == cudaMemoryTypeManaged ||
-                      (p->type == cudaMemoryTypeHost && p->devicePointer == given);
-      if (!ok) return GS_ERR_ARG;
-    }
+    if (!device_reachable(tt.in[i]) || !device_reachable(tt.out[i])) return GS_ERR_ARG;
   }
   // no output may overlap any input or any other output
   if (spans_conflict(written, (size_t)tt.n, read, (size_t)tt.n)) return GS_ERR_ARG;
@@ -154,18 +142,8 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
       (skipped && ((uintptr_t)skipped & 7u)))
     return GS_ERR_ARG;
   for (const void* p : {(const void*)scale, (const void*)growth_tracker, (const void*)found_inf,
-                        (const void*)skipped}) {
-    if (!p) continue;
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-      cudaGetLastError();
-      return GS_ERR_ARG;
-    }
-    const bool ok = (a.type == cudaMemoryTypeDevice && a.device == current_device()) ||
-                    a.type == cudaMemoryTypeManaged ||
-                    (a.type == cudaMemoryTypeHost && a.devicePointer == p);
-    if (!ok) return GS_ERR_ARG;
-  }
+                        (const void*)skipped})
+    if (p && !device_reachable(p)) return GS_ERR_ARG;
   cudaError_t e = cudaSuccess;
   unsigned char* scratch = scratch_address(&e);
   if (!scratch) {
