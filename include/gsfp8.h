@@ -206,13 +206,18 @@ int gs_scaler_state_set(float* scale, int32_t* growth_tracker, float h_scale,
  * the process exits).  Limits: at most 960 tensors and 32768 chunks of 8192
  * elements (268,435,456 elements in total); larger lists return
  * GS_ERR_SHAPE before anything is launched (see gs_noalloc_limits).
- * The call makes no cudaMalloc / cudaFree and allocates nothing.  Its first
- * call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current): make that first call before any stream capture.
- * Every call shares the one array and its contents persist between calls; the
- * call clears what must start at zero itself.  Calls that overlap on the GPU
- * (on different streams, or from different host threads without ordering)
- * race on the array: order them on one stream. */
+ * The call makes no cudaMalloc / cudaFree and allocates nothing; it uses
+ * about 62 KB of the calling thread's stack for the tensor table it passes to
+ * the GPU.  Its first call in a CUDA context looks up the array's device
+ * address there (cudaGetSymbolAddress) and caches it under the context's ID:
+ * each device's primary context, the new primary context that follows a
+ * cudaDeviceReset, and any context the caller creates has its own copy of the
+ * array and makes its own first call.  Make that first call before any
+ * stream capture.  Every call in a context shares that context's array, and
+ * its contents persist between calls; the call clears what must start at
+ * zero itself.  Calls that overlap on the GPU (on different streams, or from
+ * different host threads without ordering) race on the array: order them on
+ * one stream. */
 int gs_unscale_check_update_noalloc(const void* const* grads, void* const* outs,
                                     const int64_t* numels, int32_t n_tensors, float* scale,
                                     int32_t* growth_tracker, int32_t* found_inf, int64_t* skipped,

@@ -133,3 +133,115 @@ def test_noalloc_flat_buffer_equals_list(gs):
         runs.append((fout.view(torch.int32).clone(), [t.item() for t in state]))
     assert torch.equal(runs[0][0], runs[1][0])
     assert runs[0][1] == runs[1][1]
+
+
+# Run in a fresh process: two CUDA contexts on device 0, created with the
+# driver API, both alive; the allocation-free step runs in A, then in B, then
+# in A again, each time beside gs_unscale_check_update on the same inputs.
+# Each context holds its own copy of the library's scratch array, so a call
+# in B must not reuse the address looked up in A.
+_TWO_CONTEXTS = r'''
+import ctypes, sys
+import numpy as np
+cu = ctypes.CDLL("libcuda.so.1")
+lib = ctypes.CDLL(sys.argv[1])
+vp, u64, i64, i32, f32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+
+def ck(r, what):
+    if r != 0:
+        raise SystemExit(f"{what} returned {r}")
+
+class CtxParams(ctypes.Structure):
+    _fields_ = [("exec_affinity", vp), ("n_exec_affinity", ctypes.c_int), ("cig", vp)]
+
+ck(cu.cuInit(0), "cuInit")
+dev = ctypes.c_int()
+ck(cu.cuDeviceGet(ctypes.byref(dev), 0), "cuDeviceGet")
+ctxs = []
+for _ in range(2):
+    c = vp()
+    ck(cu.cuCtxCreate_v4(ctypes.byref(c), ctypes.byref(CtxParams()), 0, dev), "cuCtxCreate")
+    ctxs.append(c)
+cu.cuMemcpyHtoD_v2.argtypes = [u64, vp, ctypes.c_size_t]
+cu.cuMemcpyDtoH_v2.argtypes = [vp, u64, ctypes.c_size_t]
+cu.cuCtxSetCurrent.argtypes = [vp]
+lib.gs_tensor_list_create.argtypes = [vp, vp, vp, i32, ctypes.POINTER(vp)]
+lib.gs_tensor_list_destroy.argtypes = [vp]
+lib.gs_unscale_check_update.argtypes = [vp, u64, u64, u64, u64, f32, f32, i32, vp]
+lib.gs_unscale_check_update_noalloc.argtypes = [vp, vp, vp, i32, u64, u64, u64, u64, f32, f32,
+                                                i32, vp]
+
+def dalloc(nbytes):
+    p = u64()
+    ck(cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(max(nbytes, 16))), "cuMemAlloc")
+    return p.value
+
+def put(d, arr):
+    arr = np.ascontiguousarray(arr)
+    ck(cu.cuMemcpyHtoD_v2(d, arr.ctypes.data, arr.nbytes), "cuMemcpyHtoD")
+
+def get(d, like):
+    out = np.empty_like(like)
+    ck(cu.cuMemcpyDtoH_v2(out.ctypes.data, d, out.nbytes), "cuMemcpyDtoH")
+    return out
+
+sizes = [300007, 8191, 1, 65536, 12345]
+rng = np.random.default_rng(5)
+for call, ci in enumerate([0, 1, 0]):
+    ck(cu.cuCtxSetCurrent(ctxs[ci]), "cuCtxSetCurrent")
+    hosts = [(rng.standard_normal(n) * 300).astype(np.float16) for n in sizes]
+    if call == 1:
+        hosts[3][777] = np.inf
+    g = [dalloc(2 * n) for n in sizes]
+    o_ref = [dalloc(4 * n) for n in sizes]
+    o_new = [dalloc(4 * n) for n in sizes]
+    for d, h in zip(g, hosts):
+        put(d, h)
+    for d, n in zip(o_new, sizes):
+        put(d, np.full(n, 123.0, np.float32))
+    states = []
+    for _ in range(2):
+        s = [dalloc(4), dalloc(4), dalloc(4), dalloc(8)]
+        put(s[0], np.array([4096.0], np.float32))
+        put(s[1], np.array([2], np.int32))
+        put(s[2], np.array([0], np.int32))
+        put(s[3], np.array([0], np.int64))
+        states.append(s)
+    k = len(sizes)
+    gp, rp, npp = (vp * k)(*g), (vp * k)(*o_ref), (vp * k)(*o_new)
+    ne = (i64 * k)(*sizes)
+    tl = vp()
+    ck(lib.gs_tensor_list_create(gp, rp, ne, k, ctypes.byref(tl)), "gs_tensor_list_create")
+    ck(lib.gs_unscale_check_update(tl, *states[0], 2.0, 0.5, 3, None), "gs_unscale_check_update")
+    ck(lib.gs_unscale_check_update_noalloc(gp, npp, ne, k, *states[1], 2.0, 0.5, 3, None),
+       "gs_unscale_check_update_noalloc")
+    ck(cu.cuCtxSynchronize(), "cuCtxSynchronize")
+    for t, n in enumerate(sizes):
+        a = get(o_new[t], np.empty(n, np.uint32))
+        b = get(o_ref[t], np.empty(n, np.uint32))
+        if not np.array_equal(a, b):
+            raise SystemExit(f"call {call} (context {ci}) tensor {t}: outputs differ")
+    like = [np.empty(1, np.float32), np.empty(1, np.int32), np.empty(1, np.int32),
+            np.empty(1, np.int64)]
+    got = [get(d, l).item() for d, l in zip(states[1], like)]
+    want = [get(d, l).item() for d, l in zip(states[0], like)]
+    if got != want:
+        raise SystemExit(f"call {call} (context {ci}): state {got} != {want}")
+    if want[2] != (1 if call == 1 else 0):
+        raise SystemExit(f"call {call}: found_inf {want[2]}")
+    ck(lib.gs_tensor_list_destroy(tl), "gs_tensor_list_destroy")
+print("ok")
+'''
+
+
+def test_noalloc_each_context_uses_its_own_array(gs):
+    """A process that runs the step in two CUDA contexts on one device (two
+    contexts a caller created, alive at once): each call matches
+    gs_unscale_check_update in the same context, so no context is handed
+    the array address another context looked up."""
+    import os
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-c", _TWO_CONTEXTS, gs.lib_path()], capture_output=True,
+                       text=True, timeout=300, env=dict(os.environ))
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
