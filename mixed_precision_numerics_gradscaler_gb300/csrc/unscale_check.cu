@@ -10,7 +10,7 @@
 // Optionally (step 5's clipping needs it) the same pass returns the global
 // L2 norm of the unscaled gradients.
 //
-// Layout: an oversubscribed grid (32 CTAs per SM, four or more waves of
+// Layout: an oversubscribed grid (kUnscaleCtasPerSm CTAs per SM, several waves of
 // resident CTAs) walks the list's chunk table grid-stride.  A full 8192-
 // element chunk is one pass of a 256-thread CTA: each thread issues two
 // 32-byte loads (16 FP16 each) and four 32-byte stores (8 FP32 each).
