@@ -12,13 +12,17 @@ synthetic inputs resident in HBM:
 value = algorithmic HBM bytes of the step / device time (GB/s).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--sweep] [--no-e2e] [--only KERNEL]
+                       [--sweep] [--no-e2e] [--no-extra] [--only KERNEL]
 Under torchrun (N > 1) every rank runs its own replica of the step on its
 own GPU (no data-path collective); rank 0 prints one JSON line.
+At N = 1 the line also carries, timed after the step and outside `value`:
+`sweep` (the unscale and 1x128 quantiser at 1 MiB, 128 MiB, 2 GiB and
+8 GiB) and `kernels_extra` (MXFP8 quantise / dequantise, delayed E5M2, the
+norm form of the unscale, the master update, and the FP8 GEMM in TFLOP/s
+against the FP8 tensor peak).
 --impl reference times the CPU oracle on the host threads (the pages ship no
-implementation); --sweep runs the 1 MiB .. 8 GiB bandwidth sweep; --only
-times one kernel alone (the rows beyond the step, and the FP8 GEMM in
-TFLOP/s against the FP8 tensor peak).
+implementation); --sweep runs every point of the 1 MiB .. 8 GiB bandwidth
+sweep; --only times one kernel alone.
 """
 from __future__ import annotations
 
@@ -63,11 +67,10 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=6)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--only", choices=["unscale", "quant_1x128", "dequant", "quant_128x128",
-                                      "quant_128x128_tma",
-                                      "quant_tensor", "quant_mx", "dequant_mx", "quant_delayed",
-                                      "unscale_norm", "master_update", "gemm"],
+    p.add_argument("--only", choices=ONLY_CASES,
                    help="time one kernel alone on a small case (for ncu captures)")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the sweep points and the rows beyond the step after the step")
     return p.parse_args(argv)
 
 
@@ -376,6 +379,18 @@ class Workload:
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.h_in)
         self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.h_out)
 
+    def release(self):
+        """Frees every device and pinned host buffer of the step."""
+        for d in getattr(self, "sets", []):
+            if d["tl"] is not self.tl:
+                d["tl"].close()
+        self.tl.close()
+        self.sets = []
+        self.h_in = self.h_out = None
+        self.grads = self.outs = None
+        self.x3 = self.q3 = self.s3 = self.y3 = self.x4 = self.q4 = self.s4 = None
+        self.x5 = self.q5 = self.s5 = self.ws = None
+
     def _step_on(self, d, k):
         gs = self.gs
         st = self.torch.cuda.current_stream().cuda_stream
@@ -601,6 +616,7 @@ def run_ours(args):
             dist.barrier()
     elapsed = t_start.elapsed_time(t_end) / 1000.0
     max_el, total_bytes = aggregate(elapsed, float(w.bytes_per_step * args.steps), dist, dev)
+    launches = w.launches_per_step * args.steps
     value = throughput(total_bytes, max_el)
 
     per = {}
@@ -647,6 +663,16 @@ def run_ours(args):
                            "overlap step k (copy-in, compute and copy-out streams)"}
 
     cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1) else None
+    sweep = extra = None
+    if world == 1 and not args.no_extra:
+        scale_after, skipped_after = float(w.scale.item()), int(w.skipped.item())
+        w.release()
+        del w
+        torch.cuda.empty_cache()
+        sweep = sweep_points(torch, gs, SWEEP_BENCH_SIZES, args.warmup)
+        extra = kernels_extra(torch, gs, args.warmup)
+    else:
+        scale_after, skipped_after = float(w.scale.item()), int(w.skipped.item())
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1000 * max_el / args.steps,
@@ -656,92 +682,114 @@ def run_ours(args):
                            "l2": "no flush: every input (16 GB, 268 MB, 470 MB, 470 MB) is larger "
                                  "than the 129 MB L2", "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": w.launches_per_step * args.steps,
+                "gpu_launches": launches,
                 "clocks": clocks.summary(), "kernels": kernels,
-                "state_after": {"scale": float(w.scale.item()), "skipped": int(w.skipped.item())}}
+                "state_after": {"scale": scale_after, "skipped": skipped_after},
+                "sweep": sweep, "kernels_extra": extra}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
 
 
-def run_sweep(args):
-    """Config 5: GB/s of unscale (one flat fp16 tensor) and of 1x128 E4M3
-    quantisation (bf16 [bytes/16384, 8192]) for inputs of 1 MiB .. 8 GiB."""
-    import torch
+# ---- config 5: the bandwidth sweep ---------------------------------------------
+
+SWEEP_BENCH_SIZES = [1 << 20, 1 << 27, 1 << 31, 1 << 33]   # the points in the default line
+
+
+def sweep_points(torch, gs, sizes, warmup: int, reps: int = 10) -> list:
+    """GB/s of unscale (one flat fp16 tensor, config 2's distribution) and of
+    1x128 E4M3 quantisation (bf16 [bytes/16384, 8192], config 3's
+    distribution) for inputs of the given byte sizes; L2 flushed (a 512 MiB
+    buffer zeroed) before every timed launch; median of `reps` launches."""
     import datagen as dg
     from datagen import workloads as wl
-    import mixed_precision_numerics_gradscaler_gb300 as gs
-    torch.cuda.set_device(0)
     st = torch.cuda.current_stream().cuda_stream
-    peak, src = hbm_peak()
+    peak, _ = hbm_peak()
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+
+    def timed(fn):
+        ts = []
+        for r in range(max(warmup, 3) + reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= max(warmup, 3):
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
     points = []
-    for nbytes in wl.cfg5_sizes():
+    for nbytes in sizes:
+        res = {"input_bytes": nbytes, "cache_resident": nbytes < 2 * 129 * 2 ** 20}
         n = nbytes // 2
         g = torch.empty(n, dtype=torch.float16, device="cuda")
-        lo, hi = wl.binades(-10, -1, 16)
-        dg.fill_device(dg.logu_f16(wl.seed_of(5), 0, lo, hi), 0, n, g.data_ptr(), st)
+        dg.fill_device(wl.cfg5_grad_spec(), 0, n, g.data_ptr(), st)
         o = torch.empty(n, dtype=torch.float32, device="cuda")
         tl = gs.gs_tensor_list_create([g], [o])
         sc = torch.tensor([65536.0], device="cuda")
         tr = torch.zeros(1, dtype=torch.int32, device="cuda")
         fi = torch.zeros(1, dtype=torch.int32, device="cuda")
-        x = g.view(torch.bfloat16).view(-1, 8192) if n % 8192 == 0 else None
-        res = {"input_bytes": nbytes, "cache_resident": nbytes < 2 * 129 * 2 ** 20}
-        for name, fn, b in [
-            ("unscale", lambda: gs.gs_unscale_check_update(tl, sc, tr, fi, None, 2.0, 0.5, 2000), 6 * n)]:
-            ts = []
-            for r in range(max(args.warmup, 3) + 10):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                fn()
-                e1.record()
-                torch.cuda.synchronize()
-                if r >= max(args.warmup, 3):
-                    ts.append(e0.elapsed_time(e1))
-            ms = statistics.median(ts)
-            res[name] = {"ms": ms, "gbs": b / ms / 1e6, "frac": b / ms / 1e6 / peak}
-        if x is not None:
-            q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
-            s = torch.empty(x.shape[0], 64, dtype=torch.float32, device="cuda")
-            nb = 3 * n + 4 * (n // 128)
-            ts = []
-            for r in range(max(args.warmup, 3) + 10):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)
-                e1.record()
-                torch.cuda.synchronize()
-                if r >= max(args.warmup, 3):
-                    ts.append(e0.elapsed_time(e1))
-            ms = statistics.median(ts)
-            res["quant_1x128"] = {"ms": ms, "gbs": nb / ms / 1e6, "frac": nb / ms / 1e6 / peak}
-            del q, s
-        points.append(res)
+        ms = timed(lambda: gs.gs_unscale_check_update(tl, sc, tr, fi, None, 2.0, 0.5, 2000))
+        b = 6 * n
+        res["unscale"] = {"ms": round(ms, 5), "gbs": round(b / ms / 1e6, 1),
+                          "frac": round(b / ms / 1e6 / peak, 4)}
         tl.close()
-        del g, o
+        del g, o, tl
         torch.cuda.empty_cache()
+        a = wl.cfg5_act(nbytes)
+        x = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device="cuda")
+        dg.fill_device(a.spec, 0, a.numel, x.data_ptr(), st)
+        q = torch.empty(a.rows, a.cols, dtype=torch.uint8, device="cuda")
+        s = torch.empty(a.rows, a.cols // 128, dtype=torch.float32, device="cuda")
+        ms = timed(lambda: gs.fp8_quant_block(x, 1, 128, "e4m3", q, s))
+        b = 3 * a.numel + 4 * (a.numel // 128)
+        res["quant_1x128"] = {"ms": round(ms, 5), "gbs": round(b / ms / 1e6, 1),
+                              "frac": round(b / ms / 1e6 / peak, 4)}
+        del x, q, s
+        torch.cuda.empty_cache()
+        points.append(res)
+    del flush
+    torch.cuda.empty_cache()
+    return points
+
+
+def run_sweep(args):
+    """Config 5: every size of the sweep, 1 MiB .. 8 GiB."""
+    import torch
+    from datagen import workloads as wl
+    import mixed_precision_numerics_gradscaler_gb300 as gs
+    torch.cuda.set_device(0)
+    peak, src = hbm_peak()
+    points = sweep_points(torch, gs, wl.cfg5_sizes(), args.warmup)
     print(json.dumps({"metric": METRIC, "unit": UNIT, "peak": peak, "peak_source": src,
                       "l2": "512 MiB buffer zeroed before every timed launch", "sweep": points}))
     return 0
 
 
-def run_only(args):
-    """One kernel alone, on a case small enough for a full ncu capture: the
-    unscale on the first two layers of the Llama-3-8B list (18 tensors,
-    436 M elements: 0.87 GB in, 1.7 GB out); the FP8 kernels on their own
-    configs (268-470 MB of input)."""
-    import torch
+# ---- one kernel alone --------------------------------------------------------------
+
+ONLY_CASES = ["unscale", "quant_1x128", "dequant", "quant_128x128", "quant_128x128_tma",
+              "quant_tensor", "quant_mx", "dequant_mx", "quant_delayed", "unscale_norm",
+              "master_update", "gemm"]
+# the rows beyond the step, timed after it in the default run
+EXTRA_CASES = ["quant_mx", "dequant_mx", "quant_delayed", "unscale_norm", "master_update", "gemm"]
+
+
+def kernel_case(torch, gs, name: str) -> dict:
+    """Buffers and the launch of one kernel on its own workload: the unscale
+    forms and the master update on the first two layers of the Llama-3-8B
+    list (18 tensors, 436 M elements); the quantisers on their configs
+    (268-470 MB of input); the FP8 GEMM on activations [16384, 8192] times a
+    weight [28672, 8192].  Returns {"fn", "bytes" (algorithmic, per launch)
+    or "flops", "workload"}."""
     import datagen as dg
     from datagen import workloads as wl
-    import mixed_precision_numerics_gradscaler_gb300 as gs
-    torch.cuda.set_device(0)
     st = torch.cuda.current_stream().cuda_stream
     dev = "cuda"
-    if args.only in ("unscale_norm", "master_update"):
+    if name in ("unscale", "unscale_norm", "master_update"):
         cfg = wl.cfg2_grads()
         n_t = 18
         grads = [torch.empty(n, dtype=torch.float16, device=dev) for n in cfg.numels[:n_t]]
@@ -753,59 +801,45 @@ def run_only(args):
         tr = torch.zeros(1, dtype=torch.int32, device=dev)
         fi = torch.zeros(1, dtype=torch.int32, device=dev)
         nrm = torch.empty(1, dtype=torch.float32, device=dev)
-        gs.gs_unscale_check_update_norm(tl, sc, tr, fi, nrm, None, 2.0, 0.5, 2000)
         n_par = sum(cfg.numels[:n_t])
-        if args.only == "unscale_norm":
-            fn = lambda: gs.gs_unscale_check_update_norm(tl, sc, tr, fi, nrm, None, 2.0, 0.5, 2000)
-            nbytes = 6 * n_par
-        else:
-            w32 = [torch.zeros(n, dtype=torch.float32, device=dev) for n in cfg.numels[:n_t]]
-            wbf = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for n in cfg.numels[:n_t]]
-            pl = gs.gs_param_list_create(w32, outs, wbf)
-            fn = lambda: gs.gs_master_update_sgd(pl, 1e-4, 1.0, nrm, fi)
-            nbytes = 14 * n_par
-    elif args.only == "unscale":
-        cfg = wl.cfg2_grads()
-        n_t = 18
-        grads = [torch.empty(n, dtype=torch.float16, device=dev) for n in cfg.numels[:n_t]]
-        outs = [torch.empty(n, dtype=torch.float32, device=dev) for n in cfg.numels[:n_t]]
-        for t, g in enumerate(grads):
-            dg.fill_device(cfg.spec(t, 0), 0, g.numel(), g.data_ptr(), st)
-        tl = gs.gs_tensor_list_create(grads, outs)
-        sc = torch.tensor([65536.0], device=dev)
-        tr = torch.zeros(1, dtype=torch.int32, device=dev)
-        fi = torch.zeros(1, dtype=torch.int32, device=dev)
-        fn = lambda: gs.gs_unscale_check_update(tl, sc, tr, fi, None, 2.0, 0.5, 2000)
-        nbytes = 6 * sum(cfg.numels[:n_t])
-    elif args.only in ("quant_1x128", "dequant"):
+        wk = "Llama-3-8B grads, first 2 layers (18 tensors, %d elems)" % n_par
+        if name == "unscale":
+            return {"fn": lambda: gs.gs_unscale_check_update(tl, sc, tr, fi, None, 2.0, 0.5, 2000),
+                    "bytes": 6 * n_par, "workload": wk, "keep": (grads, outs, tl)}
+        gs.gs_unscale_check_update_norm(tl, sc, tr, fi, nrm, None, 2.0, 0.5, 2000)
+        if name == "unscale_norm":
+            return {"fn": lambda: gs.gs_unscale_check_update_norm(tl, sc, tr, fi, nrm, None, 2.0,
+                                                                  0.5, 2000),
+                    "bytes": 6 * n_par, "workload": wk, "keep": (grads, outs, tl)}
+        w32 = [torch.zeros(n, dtype=torch.float32, device=dev) for n in cfg.numels[:n_t]]
+        wbf = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for n in cfg.numels[:n_t]]
+        pl = gs.gs_param_list_create(w32, outs, wbf)
+        return {"fn": lambda: gs.gs_master_update_sgd(pl, 1e-4, 1.0, nrm, fi),
+                "bytes": 14 * n_par, "workload": wk + ", SGD on fp32 masters + bf16 copies",
+                "keep": (grads, outs, tl, w32, wbf, pl)}
+    if name in ("quant_1x128", "dequant", "quant_mx", "dequant_mx"):
         a = wl.cfg3_act()
         x = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
         dg.fill_device(a.spec, 0, a.numel, x.data_ptr(), st)
         q = torch.empty(a.rows, a.cols, dtype=torch.uint8, device=dev)
-        s = torch.empty(a.rows, a.cols // 128, dtype=torch.float32, device=dev)
         y = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
-        gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)
-        if args.only == "quant_1x128":
-            fn = lambda: gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)
-        else:
-            fn = lambda: gs.fp8_dequant(q, s, 1, 128, "e4m3", y)
-        nbytes = 3 * a.numel + 4 * (a.numel // 128)
-    elif args.only in ("quant_mx", "dequant_mx"):
-        a = wl.cfg3_act()
-        x = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
-        dg.fill_device(a.spec, 0, a.numel, x.data_ptr(), st)
-        q = torch.empty(a.rows, a.cols, dtype=torch.uint8, device=dev)
+        wk = "bf16 activations [16384, 8192]"
+        if name in ("quant_1x128", "dequant"):
+            s = torch.empty(a.rows, a.cols // 128, dtype=torch.float32, device=dev)
+            gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)
+            fn = (lambda: gs.fp8_quant_block(x, 1, 128, "e4m3", q, s)) if name == "quant_1x128" \
+                else (lambda: gs.fp8_dequant(q, s, 1, 128, "e4m3", y))
+            return {"fn": fn, "bytes": 3 * a.numel + 4 * (a.numel // 128),
+                    "workload": wk + (", E4M3 1x128" if name == "quant_1x128" else
+                                      ", E4M3 1x128 -> bf16"), "keep": (x, q, s, y)}
         s = torch.empty(a.rows, a.cols // 32, dtype=torch.uint8, device=dev)
-        y = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
         gs.fp8_quant_mx(x, "e4m3", q, s)
-        if args.only == "quant_mx":
-            fn = lambda: gs.fp8_quant_mx(x, "e4m3", q, s)
-        else:
-            fn = lambda: gs.fp8_dequant_mx(q, s, "e4m3", y)
-        nbytes = 3 * a.numel + a.numel // 32
-    elif args.only == "gemm":
-        # the consumer: activations [16384 tokens, 8192] (1x128 E4M3 tiles)
-        # times a weight [28672, 8192] (128x128 E4M3 tiles), bf16 out
+        fn = (lambda: gs.fp8_quant_mx(x, "e4m3", q, s)) if name == "quant_mx" \
+            else (lambda: gs.fp8_dequant_mx(q, s, "e4m3", y))
+        return {"fn": fn, "bytes": 3 * a.numel + a.numel // 32,
+                "workload": wk + (", MXFP8 E4M3" if name == "quant_mx" else ", MXFP8 E4M3 -> bf16"),
+                "keep": (x, q, s, y)}
+    if name == "gemm":
         a = wl.cfg3_act()
         w = wl.cfg4_weight(rows=28672, cols=8192)
         x = torch.empty(a.rows, a.cols, dtype=torch.bfloat16, device=dev)
@@ -820,49 +854,53 @@ def run_only(args):
         gs.fp8_quant_block(wt, 128, 128, "e4m3", qb, sb)
         del x, wt
         d = torch.empty(a.rows, w.rows, dtype=torch.bfloat16, device=dev)
-        fn = lambda: gs.fp8_gemm_block_scaled(qa, sa, qb, sb, "e4m3", d)
-        flops = 2 * a.rows * w.rows * a.cols
-        nbytes = None
-    elif args.only in ("quant_128x128", "quant_128x128_tma"):
+        return {"fn": lambda: gs.fp8_gemm_block_scaled(qa, sa, qb, sb, "e4m3", d),
+                "flops": 2 * a.rows * w.rows * a.cols,
+                "workload": "E4M3 [16384, 8192] (1x128 scales) x [28672, 8192]^T (128x128 "
+                            "scales) -> bf16", "keep": (qa, sa, qb, sb, d)}
+    if name in ("quant_128x128", "quant_128x128_tma"):
         w = wl.cfg4_weight()
         # the TMA-staged kernel takes inputs 16-byte but not 32-byte aligned
-        off = 8 if args.only == "quant_128x128_tma" else 0
+        off = 8 if name == "quant_128x128_tma" else 0
         xbuf = torch.empty(w.numel + off, dtype=torch.bfloat16, device=dev)
         x = xbuf[off:].view(w.rows, w.cols)
         dg.fill_device(w.spec, 0, w.numel, x.data_ptr(), st)
         q = torch.empty(w.rows, w.cols, dtype=torch.uint8, device=dev)
         s = torch.empty(w.rows // 128, w.cols // 128, dtype=torch.float32, device=dev)
-        fn = lambda: gs.fp8_quant_block(x, 128, 128, "e4m3", q, s)
-        nbytes = 3 * w.numel + 4 * (w.numel // 16384)
-    elif args.only == "quant_delayed":
-        g = wl.cfg4_grad()
-        x = torch.empty(g.numel, dtype=torch.bfloat16, device=dev)
-        dg.fill_device(g.spec, 0, g.numel, x.data_ptr(), st)
-        q = torch.empty(g.numel, dtype=torch.uint8, device=dev)
+        return {"fn": lambda: gs.fp8_quant_block(x, 128, 128, "e4m3", q, s),
+                "bytes": 3 * w.numel + 4 * (w.numel // 16384),
+                "workload": "bf16 weight 8192x28672, E4M3 128x128" +
+                            (" (input 16-byte aligned)" if off else ""), "keep": (xbuf, q, s)}
+    g = wl.cfg4_grad()
+    x = torch.empty(g.numel, dtype=torch.bfloat16, device=dev)
+    dg.fill_device(g.spec, 0, g.numel, x.data_ptr(), st)
+    q = torch.empty(g.numel, dtype=torch.uint8, device=dev)
+    ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=dev)
+    if name == "quant_delayed":
         hist = torch.full((16,), 1e-2, dtype=torch.float32, device=dev)
         pos = torch.zeros(1, dtype=torch.int32, device=dev)
         used = torch.empty(1, dtype=torch.float32, device=dev)
-        ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=dev)
-        fn = lambda: gs.fp8_quant_tensor_delayed(x, "e5m2", q, hist, pos, used, ws)
-        nbytes = 3 * g.numel + 4
-    else:
-        g = wl.cfg4_grad()
-        x = torch.empty(g.numel, dtype=torch.bfloat16, device=dev)
-        dg.fill_device(g.spec, 0, g.numel, x.data_ptr(), st)
-        q = torch.empty(g.numel, dtype=torch.uint8, device=dev)
-        s = torch.empty(1, dtype=torch.float32, device=dev)
-        ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=dev)
-        fn = lambda: gs.fp8_quant_tensor(x, "e5m2", q, s, ws)
-        nbytes = 5 * g.numel + 4
-    for _ in range(args.warmup):
+        return {"fn": lambda: gs.fp8_quant_tensor_delayed(x, "e5m2", q, hist, pos, used, ws),
+                "bytes": 3 * g.numel + 4,
+                "workload": "bf16 gradient 8192x28672, E5M2 delayed (history of 16)",
+                "keep": (x, q, ws, hist, pos, used)}
+    s = torch.empty(1, dtype=torch.float32, device=dev)
+    return {"fn": lambda: gs.fp8_quant_tensor(x, "e5m2", q, s, ws), "bytes": 5 * g.numel + 4,
+            "workload": "bf16 gradient 8192x28672, E5M2 per-tensor (two passes)",
+            "keep": (x, q, ws, s)}
+
+
+def time_case(torch, case: dict, warmup: int, iters: int, reps: int = 10) -> dict:
+    """Median per-launch time of `reps` back-to-back launches between two
+    events (host launch latency stays outside the interval; every input
+    exceeds L2), over `iters` iterations, with the SM clocks sampled."""
+    fn = case["fn"]
+    for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    # back-to-back launches between two events, so that host launch latency
-    # does not land inside the interval (inputs exceed L2: no flush needed)
-    reps = 10
     ts = []
-    with ClockSampler(gpu_uuid(torch, 0)) as clocks:
-        for _ in range(args.steps):
+    with ClockSampler(gpu_uuid(torch, torch.cuda.current_device())) as clocks:
+        for _ in range(iters):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             fn()
             e0.record()
@@ -872,19 +910,51 @@ def run_only(args):
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1) / reps)
     ms = statistics.median(ts)
-    clk = clocks.summary()
-    if nbytes is None:  # tensor-bound: FLOP/s against the FP8 peak
-        peak, src = fp8_peak(sum(ts) * reps / 1e3)
-        tf = flops / ms / 1e9
-        print(json.dumps({"only": args.only, "flops": flops, "median_ms": ms, "tflops": tf,
-                          "frac": tf / peak, "peak_tflops": peak, "peak_source": src,
-                          "gpu_status": gs.gs_device_status(), "clocks": clk,
-                          "steps": args.steps}), flush=True)
-        return 0
-    peak, src = hbm_peak()
-    print(json.dumps({"only": args.only, "bytes": nbytes, "median_ms": ms, "gbs": nbytes / ms / 1e6,
-                      "frac": nbytes / ms / 1e6 / peak, "peak": peak, "peak_source": src,
-                      "clocks": clk, "steps": args.steps}), flush=True)
+    out = {"workload": case["workload"], "median_ms": round(ms, 5), "iters": iters,
+           "launches_timed": iters * reps, "timed_s": round(sum(ts) * reps / 1e3, 3),
+           "clocks": clocks.summary()}
+    if "flops" in case:
+        peak_s, src_s = fp8_peak(1.0)
+        peak_b, src_b = fp8_peak(0.0)
+        tf = case["flops"] / ms / 1e9
+        first = case["flops"] / ts[0] / 1e9
+        out.update({"flops": case["flops"], "tflops": round(tf, 1), "peak_tflops": peak_s,
+                    "frac": round(tf / peak_s, 4), "peak_source": src_s,
+                    "tflops_first_iter": round(first, 1), "peak_burst_tflops": peak_b,
+                    "frac_burst": round(first / peak_b, 4)})
+    else:
+        peak, src = hbm_peak()
+        gbs = case["bytes"] / ms / 1e6
+        out.update({"bytes": case["bytes"], "gbs": round(gbs, 1), "peak": peak,
+                    "frac": round(gbs / peak, 4), "peak_source": src})
+    return out
+
+
+def kernels_extra(torch, gs, warmup: int) -> dict:
+    """The rows beyond the step, each timed alone after it: MXFP8 quantise and
+    dequantise, delayed E5M2, the norm form of the unscale, the master
+    update, and the FP8 GEMM (timed for about a second, against the sustained
+    FP8 peak)."""
+    out = {}
+    for name in EXTRA_CASES:
+        case = kernel_case(torch, gs, name)
+        out[name] = time_case(torch, case, max(warmup, 3), 40 if name == "gemm" else 10)
+        del case
+        torch.cuda.empty_cache()
+    out["gpu_status"] = gs.gs_device_status()
+    return out
+
+
+def run_only(args):
+    """One kernel alone, on a case small enough for a full ncu capture."""
+    import torch
+    import mixed_precision_numerics_gradscaler_gb300 as gs
+    torch.cuda.set_device(0)
+    case = kernel_case(torch, gs, args.only)
+    r = time_case(torch, case, args.warmup, args.steps)
+    r["only"] = args.only
+    r["gpu_status"] = gs.gs_device_status()
+    print(json.dumps(r), flush=True)
     return 0
 
 

@@ -157,3 +157,24 @@ def cfg4_grad(rows: int = 8192, cols: int = 28672) -> QuantInput:
 def cfg5_sizes() -> list[int]:
     """Input sizes of the bandwidth sweep: 1 MiB .. 8 GiB, powers of two."""
     return [1 << k for k in range(20, 34)]
+
+
+def cfg5_grad_spec() -> Spec:
+    """The sweep's unscale input: one flat fp16 tensor with config 2's
+    distribution (|g| = 10^U(-10,-1) * 2^16, random sign)."""
+    lo, hi = binades(-10, -1, 16)
+    return logu_f16(seed_of(5), 0, lo, hi)
+
+
+def cfg5_act(nbytes: int) -> QuantInput:
+    """The sweep's 1x128 E4M3 input of `nbytes` bytes: bf16 [nbytes / 16384,
+    8192] with config 3's distribution (N(0,1), 4 outlier channels x
+    log-U(100, 3000))."""
+    cols = 8192
+    rows = max(1, nbytes // (2 * cols))
+    rng = np.random.default_rng(seed_of(5))
+    chans = rng.choice(cols, size=4, replace=False)
+    mults = np.exp(rng.uniform(math.log(100.0), math.log(3000.0), size=4)).astype(np.float32)
+    s = normal_bf16(seed_of(5), 1, 1.0, cols, chans=list(zip(chans.tolist(), mults.tolist())))
+    return QuantInput("cfg5_act", rows, cols, s, (1, 128), "e4m3",
+                      {"outlier_channels": chans.tolist(), "multipliers": mults.tolist()})

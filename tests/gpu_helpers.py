@@ -1,4 +1,7 @@
 """Helpers shared by the GPU parity tests (test infrastructure)."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -49,3 +52,17 @@ def assert_same_bytes(got, want, what=""):
         i = np.flatnonzero(~ok.ravel())[:5]
         raise AssertionError(f"{what}: {(~ok).sum()} mismatches, first at {i.tolist()}: "
                              f"got {[hex(v) for v in got.ravel()[i]]} want {[hex(v) for v in want.ravel()[i]]}")
+
+
+def host_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except Exception:
+        return max(1, os.cpu_count() or 1)
+
+
+def pmap(fn, items):
+    """fn over items on every host core (the input generator and the oracle
+    are C behind ctypes, which releases the GIL)."""
+    with ThreadPoolExecutor(max_workers=host_threads()) as ex:
+        return list(ex.map(fn, items))

@@ -6,7 +6,7 @@ import torch
 
 import datagen as dg
 from datagen import workloads as wl
-from gpu_helpers import DEV, assert_same_bytes, assert_same_f32, bits_of, same_bf16, to_dev16
+from gpu_helpers import DEV, assert_same_bytes, assert_same_f32, bits_of, pmap, same_bf16, to_dev16
 
 pytestmark = pytest.mark.gpu
 
@@ -186,13 +186,13 @@ def _torch_reference_1x128(xd, fmt):
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
-def test_exhaustive_16bit_value_and_tile_amax_pairs(gs, fmt, dt):
+def test_exhaustive_16bit_value_and_tile_amax_pairs(gs, orc, fmt, dt):
     """Every pair (x, amax) of 16-bit patterns (bf16 or f16) with |x| <= amax:
     one tile per 127 x-values holding amax itself, so each tile's scale comes
     from that amax.  Covers the fast exact-quotient path for every finite amax
     and the IEEE path for Inf/NaN amax; compared with the library composition
     of the same formula on the device (itself pinned to the oracle on the
-    CPU)."""
+    CPU), and every 61st tile directly with the oracle."""
     chunk = 512
     for a0 in range(0, 0x8000, chunk):
         a = torch.arange(a0, min(a0 + chunk, 0x8000), device=DEV, dtype=torch.int64)
@@ -218,6 +218,11 @@ def test_exhaustive_16bit_value_and_tile_amax_pairs(gs, fmt, dt):
         assert bool(same_s.all()), f"scales differ near amax {a0}"
         bad = (q.view(-1) != rq).nonzero()
         assert bad.numel() == 0, (a0, bad[:5].view(-1).tolist(), xd.view(-1)[bad[:5].view(-1)].tolist())
+        sub = torch.arange(a0 % 61, n_t, 61, device=DEV)
+        xs = xd[sub].view(torch.int16).cpu().numpy().view(np.uint16)
+        oq, os_ = orc.quant_block(xs, 1, 128, FMT[fmt], dtype=ODT[dt])
+        assert_same_bytes(q[sub].cpu().numpy(), oq, f"oracle, tiles near amax {a0}")
+        assert_same_f32(s[sub].cpu().numpy(), os_, f"oracle scales near amax {a0}")
 
 
 def test_cfg3_full_size_sampled(gs, orc):
@@ -257,11 +262,11 @@ def test_cfg3_full_size_sampled(gs, orc):
     assert float(s.max()) > 100 / 448
 
 
-def test_cfg4_weight_128x128_full_size_sampled(gs, orc):
+def test_cfg4_weight_128x128_full_size(gs, orc):
     """Config 4 weights: bf16 8192x28672 N(0,0.02), 14 hot blocks x100, E4M3
-    128x128 through the TMA kernel; every hot block and 40 random blocks are
-    recomputed by the oracle; all 14336 scales are checked against the
-    library amax of the same blocks."""
+    128x128 (32-byte aligned input: the direct-load kernel).  The oracle
+    quantises the host-regenerated weight, one 128-row block-row per host
+    thread: every one of the 235e6 codes and 14336 scales is compared."""
     w = wl.cfg4_weight()
     st = torch.cuda.current_stream().cuda_stream
     x = torch.empty(w.rows, w.cols, dtype=torch.bfloat16, device=DEV)
@@ -269,21 +274,21 @@ def test_cfg4_weight_128x128_full_size_sampled(gs, orc):
     q = torch.empty(w.rows, w.cols, dtype=torch.uint8, device=DEV)
     s = torch.empty(w.rows // 128, w.cols // 128, dtype=torch.float32, device=DEV)
     gs.fp8_quant_block(x, 128, 128, "e4m3", q, s)
-    amax = x.float().view(w.rows // 128, 128, w.cols // 128, 128).abs().amax(dim=(1, 3))
-    amax = amax.clamp(min=1e-12)
-    ref_s = amax / torch.full_like(amax, 448.0)   # IEEE division (see above)
     torch.cuda.synchronize()
-    assert bool((s == ref_s).all())
-    nbc = w.cols // 128
-    rng = np.random.default_rng(9)
-    blocks = sorted(set(w.notes["hot_blocks"]) | set(rng.integers(0, s.numel(), 40).tolist()))
-    for b in blocks:
-        r0, c0 = (b // nbc) * 128, (b % nbc) * 128
-        idx = ((r0 + np.arange(128))[:, None] * w.cols + c0 + np.arange(128)[None, :]).reshape(-1)
-        xh = dg.fill_host_idx(w.spec, idx).reshape(128, 128)
-        rq, rs = orc.quant_block(xh, 128, 128, 0, dtype=1)
-        assert_same_bytes(q[r0:r0 + 128, c0:c0 + 128].cpu().numpy(), rq, f"block {b}")
-        assert_same_f32(s.view(-1)[b:b + 1].cpu().numpy(), rs.reshape(-1), f"scale {b}")
+    q_h, s_h = q.cpu().numpy(), s.cpu().numpy()
+
+    def check(br):
+        xb = dg.fill_host(w.spec, br * 128 * w.cols, 128 * w.cols).reshape(128, w.cols)
+        rq, rs = orc.quant_block(xb, 128, 128, orc.E4M3, dtype=orc.BF16)
+        return (br, int(np.count_nonzero(rq != q_h[br * 128:(br + 1) * 128])),
+                int(np.count_nonzero(rs.view(np.uint32) != s_h[br:br + 1].view(np.uint32))))
+
+    bad = [r for r in pmap(check, range(w.rows // 128)) if r[1] or r[2]]
+    assert not bad, f"block-rows (index, bad codes, bad scales) differ: {bad[:4]}"
+    # the hot blocks really carry the large scales
+    hot = np.zeros(s_h.size, bool)
+    hot[w.notes["hot_blocks"]] = True
+    assert s_h.reshape(-1)[hot].min() > 10 * s_h.reshape(-1)[~hot].max()
     assert gs.gs_device_status() == 0
 
 
