@@ -617,6 +617,7 @@ def run_ours(args):
     elapsed = t_start.elapsed_time(t_end) / 1000.0
     max_el, total_bytes = aggregate(elapsed, float(w.bytes_per_step * args.steps), dist, dev)
     launches = w.launches_per_step * args.steps
+    bytes_per_step = w.bytes_per_step
     value = throughput(total_bytes, max_el)
 
     per = {}
@@ -678,7 +679,7 @@ def run_ours(args):
                 "warmup": args.warmup, "ms_per_step": 1000 * max_el / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic (seeded counter-based generator, inputs resident in HBM)",
-                "config": {"workload": WORKLOAD, "bytes_per_step": w.bytes_per_step,
+                "config": {"workload": WORKLOAD, "bytes_per_step": bytes_per_step,
                            "l2": "no flush: every input (16 GB, 268 MB, 470 MB, 470 MB) is larger "
                                  "than the 129 MB L2", "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

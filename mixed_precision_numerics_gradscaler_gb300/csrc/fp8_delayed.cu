@@ -32,37 +32,21 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
   return m;
 }
 
-// Delayed scaling takes s from past steps, not from x, so |x| / s can pass
-// the fp32 range (a bf16 or fp32 x above FLT_MAX * s).  The IEEE quotient is
-// then +-Inf and the code saturates to +-MAX, but the exact-quotient chain
-// would meet Inf - Inf and return NaN.  Any |x| >= 2 * MAX * s saturates
-// too, so x is first clamped to +-L, L = 2 * MAX * s: every correction step
-// stays finite and no code changes.  The clamps keep NaN (min.NaN /
-// max.NaN), so a NaN input still gives the NaN code.  FP16 inputs (at most
-// 65504) cannot overflow the quotient and are not clamped.
+// Delayed scaling takes s from past steps, not from x, so x / s can leave
+// the fp32 range: a bf16 or fp32 x above FLT_MAX * s, or an infinite x of
+// any type, where the IEEE quotient is +-Inf and the clamp to +-MAX makes
+// the code +-MAX.  The exact-quotient chain would meet Inf - Inf there and
+// return NaN, so x is first clamped to +-L, L = min(2 MAX s, FLT_MAX), in
+// fp32: every |x| >= 2 MAX s gives a quotient above 2 MAX, and x = +-FLT_MAX
+// gives one of at least MAX (1 - 2^-23) since s <= FLT_MAX / MAX; all of
+// these round to +-MAX, while every |x| <= L is left as it is.  The clamp
+// keeps NaN (min.NaN / max.NaN), so a NaN input still gives the NaN code.
+// A non-finite s (a NaN or Inf in the history) takes the IEEE division,
+// which needs no clamp: its limit is +Inf, which leaves x as it is.
 template <int FMT>
 __device__ __forceinline__ float quotient_limit(float s) {
-  return __fmul_rn(2.0f * Fp8Max<FMT>::value, s);
-}
-__device__ __forceinline__ float clamp_keep_nan(float x, float lim) {
-  float d;
-  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(x), "f"(lim));
-  asm("max.NaN.f32 %0, %0, %1;" : "+f"(d) : "f"(-lim));
-  return d;
-}
-// The limit as a bf16 pair, rounded up (+Inf when it is beyond bf16's
-// range, where nothing needs clamping).
-__device__ __forceinline__ uint32_t bf16_limit2(float lim) {
-  uint16_t h;
-  asm("cvt.rp.bf16.f32 %0, %1;" : "=h"(h) : "f"(lim));
-  return (uint32_t)h * 0x10001u;
-}
-// Both bf16 halves of w clamped to +-limit (lim2 from bf16_limit2).
-__device__ __forceinline__ uint32_t clamp_bf16x2_keep_nan(uint32_t w, uint32_t lim2) {
-  uint32_t d;
-  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(lim2));
-  asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(d) : "r"(lim2 ^ 0x80008000u));
-  return d;
+  return isfinite(s) ? fminf(__fmul_rn(2.0f * Fp8Max<FMT>::value, s), 3.40282347e38f)
+                     : __int_as_float(0x7F800000);
 }
 
 // Max |h| over the history as an fp32 bit pattern; NaN entries win (their
@@ -102,9 +86,7 @@ __global__ void __launch_bounds__(kDelThreads)
   const float s = block_scale<FMT>(__uint_as_float(history_max_bits(history, hist_len, red)));
   const bool fin = isfinite(s);
   const float r = __frcp_rn(s);
-  constexpr bool kClamp = std::is_same<Tag, BF16Tag>::value;
   const float lim = quotient_limit<FMT>(s);
-  const uint32_t lim2 = bf16_limit2(lim);
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale_used = s;
   const uint32_t mm = 0x7FFF7FFFu;
   uint32_t m2 = 0;
@@ -123,10 +105,10 @@ __global__ void __launch_bounds__(kDelThreads)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       m2 = __vmaxu2(m2, __vmaxu2(a.w[j] & mm, b.w[j] & mm));
-      in[j] = kClamp ? clamp_bf16x2_keep_nan(a.w[j], lim2) : a.w[j];
-      in[8 + j] = kClamp ? clamp_bf16x2_keep_nan(b.w[j], lim2) : b.w[j];
+      in[j] = a.w[j];
+      in[8 + j] = b.w[j];
     }
-    quant_words<Tag, FMT, 16>(in, c, s, r);
+    quant_words_limited<Tag, FMT, 16>(in, c, s, r, lim);
     st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(c[0], c[1], c[2], c[3]));
     st_stream(reinterpret_cast<uint4*>(q + 16 * (v + nthreads)), make_uint4(c[4], c[5], c[6], c[7]));
     v = vn;
@@ -136,12 +118,10 @@ __global__ void __launch_bounds__(kDelThreads)
   }
   for (; v < nv; v += nthreads) {  // at most one vector left per thread
     const V8 a1 = ld_stream8(x + 32 * v);
-    uint32_t c[4], in[8];
+    uint32_t c[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) m2 = __vmaxu2(m2, __vmaxu2(a1.w[2 * j] & mm, a1.w[2 * j + 1] & mm));
-#pragma unroll
-    for (int j = 0; j < 8; ++j) in[j] = kClamp ? clamp_bf16x2_keep_nan(a1.w[j], lim2) : a1.w[j];
-    quant_words<Tag, FMT, 8>(in, c, s, r);
+    quant_words_limited<Tag, FMT, 8>(a1.w, c, s, r, lim);
     st_stream(reinterpret_cast<uint4*>(q + 16 * v), make_uint4(c[0], c[1], c[2], c[3]));
   }
   uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
@@ -152,8 +132,7 @@ __global__ void __launch_bounds__(kDelThreads)
     m = max(m, h & 0x7FFFu);
     const float f = std::is_same<Tag, BF16Tag>::value ? __uint_as_float(h << 16)
                                                        : __half2float(__ushort_as_half((unsigned short)h));
-    q[i] = (uint8_t)(quant_pair<FMT, kSteps>(0.0f, kClamp ? clamp_keep_nan(f, lim) : f, s, r, fin) &
-                     0xFFu);
+    q[i] = (uint8_t)(quant_pair<FMT, kSteps>(0.0f, clamp_keep_nan(f, lim), s, r, fin) & 0xFFu);
   }
   m = block_max_u32(m, red);
   if (threadIdx.x == 0) partials[blockIdx.x] = m;
@@ -181,29 +160,20 @@ __global__ void __launch_bounds__(kDelThreads)
   int64_t v = tid;
   for (; v + nthreads < nv; v += 2 * nthreads) {
     const V8 a = ld_stream8(x + 32 * v), b = ld_stream8(x + 32 * (v + nthreads));
-    uint32_t ia[8], ib[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      m = max(m, max(a.w[j] & mm, b.w[j] & mm));
-      ia[j] = __float_as_uint(clamp_keep_nan(__uint_as_float(a.w[j]), lim));
-      ib[j] = __float_as_uint(clamp_keep_nan(__uint_as_float(b.w[j]), lim));
-    }
+    for (int j = 0; j < 8; ++j) m = max(m, max(a.w[j] & mm, b.w[j] & mm));
     uint32_t ca[2], cb[2];
-    quant_words_f32<FMT, 8>(ia, ca, s, r);
-    quant_words_f32<FMT, 8>(ib, cb, s, r);
+    quant_words_f32_limited<FMT, 8>(a.w, ca, s, r, lim);
+    quant_words_f32_limited<FMT, 8>(b.w, cb, s, r, lim);
     st_stream(reinterpret_cast<uint2*>(q + 8 * v), make_uint2(ca[0], ca[1]));
     st_stream(reinterpret_cast<uint2*>(q + 8 * (v + nthreads)), make_uint2(cb[0], cb[1]));
   }
   for (; v < nv; v += nthreads) {
     const V8 a = ld_stream8(x + 32 * v);
-    uint32_t ia[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      m = max(m, a.w[j] & mm);
-      ia[j] = __float_as_uint(clamp_keep_nan(__uint_as_float(a.w[j]), lim));
-    }
+    for (int j = 0; j < 8; ++j) m = max(m, a.w[j] & mm);
     uint32_t ca[2];
-    quant_words_f32<FMT, 8>(ia, ca, s, r);
+    quant_words_f32_limited<FMT, 8>(a.w, ca, s, r, lim);
     st_stream(reinterpret_cast<uint2*>(q + 8 * v), make_uint2(ca[0], ca[1]));
   }
   // ragged tail (n not a multiple of 8)
@@ -243,8 +213,7 @@ __global__ void __launch_bounds__(kDelThreads)
       mag = h & 0x7FFFu;
     }
     m = max(m, mag);
-    q[i] = (uint8_t)(quant_pair<FMT, 2>(0.0f, DT == GS_F16 ? f : clamp_keep_nan(f, lim), s, r, fin) &
-                     0xFFu);
+    q[i] = (uint8_t)(quant_pair<FMT, 2>(0.0f, clamp_keep_nan(f, lim), s, r, fin) & 0xFFu);
   }
   m = block_max_u32(m, red);
   if (threadIdx.x == 0) partials[blockIdx.x] = m;

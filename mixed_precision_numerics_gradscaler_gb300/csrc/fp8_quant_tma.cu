@@ -15,8 +15,9 @@
 // mbarrier with a transaction count.  All 512 threads then pull the tile
 // from shared memory into registers (4 x 16 B each, conflict-free rows of
 // 256 B), reduce the block amax (packed 16-bit max, warp shuffle, one word
-// per warp), release the stage so the next load overlaps the cast, and
-// write FP8 codes straight from registers with 8-byte coalesced stores.
+// per warp), release the stage so the next load overlaps the cast, cast
+// through quant_words (the packed f32x2 exact quotient) and write FP8 codes
+// straight from registers with 8-byte coalesced stores.
 // Every wait on an mbarrier is bounded by %globaltimer; a CTA that gives
 // up records GS_ERR_TIMEOUT in the device status word, waits (bounded) for
 // its own loads still in flight, and returns.
@@ -28,6 +29,7 @@
 #include <mutex>
 
 #include "gs_device.cuh"
+#include "gs_quant.cuh"
 #include "gs_internal.h"
 
 namespace gs {
@@ -174,19 +176,22 @@ __global__ void __launch_bounds__(kTmaThreads)
       m = max(max(a.x, a.y), max(a.z, a.w));
     }
     const float s = block_scale<FMT>(mag16_to_float<Tag>(m));
-    const bool fin = isfinite(s);
     const float r = __frcp_rn(s);
     const int64_t r0 = br * 128, c0 = bc * 128;
     if (tid == 0) scales[br * nbc + bc] = s;
+    uint32_t in[4 * kRowPasses], c[2 * kRowPasses];
 #pragma unroll
     for (int j = 0; j < kRowPasses; ++j) {
-      uint2 o;
-      o.x = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].x), lo16<Tag>(v[j].x), s, r, fin) |
-            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].y), lo16<Tag>(v[j].y), s, r, fin) << 16);
-      o.y = quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].z), lo16<Tag>(v[j].z), s, r, fin) |
-            (quant_pair<FMT, QuotSteps<Tag>::value>(hi16<Tag>(v[j].w), lo16<Tag>(v[j].w), s, r, fin) << 16);
-      st_stream(reinterpret_cast<uint2*>(q + (r0 + row0 + kRowsPerPass * j) * C + c0 + chunk * 8), o);
+      in[4 * j] = v[j].x;
+      in[4 * j + 1] = v[j].y;
+      in[4 * j + 2] = v[j].z;
+      in[4 * j + 3] = v[j].w;
     }
+    quant_words<Tag, FMT, 4 * kRowPasses>(in, c, s, r);
+#pragma unroll
+    for (int j = 0; j < kRowPasses; ++j)
+      st_stream(reinterpret_cast<uint2*>(q + (r0 + row0 + kRowsPerPass * j) * C + c0 + chunk * 8),
+                make_uint2(c[2 * j], c[2 * j + 1]));
     advance(br, bc);
     if (++stage == kTmaStages) {
       stage = 0;

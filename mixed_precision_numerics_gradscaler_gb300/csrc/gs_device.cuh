@@ -143,6 +143,15 @@ __device__ __forceinline__ float exact_quotient(float x, float s, float r) {
   return q;
 }
 
+// x clamped to [-lim, lim] (lim >= 0), NaN kept (min.NaN / max.NaN return
+// NaN when either operand is NaN, where fminf / fmaxf would drop it).
+__device__ __forceinline__ float clamp_keep_nan(float x, float lim) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(x), "f"(lim));
+  asm("max.NaN.f32 %0, %0, %1;" : "+f"(d) : "f"(-lim));
+  return d;
+}
+
 // Quantise a pair with a finite scale (fast path) or a non-finite one (a
 // block holding Inf or NaN: IEEE division, NaN codes forced to 0x7F).
 template <int FMT, int STEPS = 2>

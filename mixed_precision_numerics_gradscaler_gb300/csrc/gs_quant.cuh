@@ -106,6 +106,36 @@ __device__ __forceinline__ void quant_words(const uint32_t* in, uint32_t* out, f
   }
 }
 
+// quant_words with every input first clamped to [-lim, lim] in fp32, NaN
+// kept (for a scale that does not bound the input: delayed scaling).  The
+// clamp acts on y = -x, which is the same interval.
+template <typename Tag, int FMT>
+__device__ __forceinline__ uint32_t quant_word_fast_limited(uint32_t w, const PackedScale& ps,
+                                                            float lim) {
+  float ylo, yhi, lo, hi;
+  upk_f32x2(neg_pair<Tag>(w), ylo, yhi);
+  const uint64_t y = pk_f32x2(clamp_keep_nan(ylo, lim), clamp_keep_nan(yhi, lim));
+  upk_f32x2(exact_quotient_x2<QuotSteps<Tag>::value>(y, ps), lo, hi);
+  return cvt_f32x2_fp8x2<FMT>(hi, lo);
+}
+template <typename Tag, int FMT, int NW>
+__device__ __forceinline__ void quant_words_limited(const uint32_t* in, uint32_t* out, float s,
+                                                    float r, float lim) {
+  static_assert(NW % 2 == 0, "words come in pairs");
+  if (isfinite(s)) {
+    const PackedScale ps = packed_scale(s, r);
+#pragma unroll
+    for (int j = 0; j < NW / 2; ++j)
+      out[j] = quant_word_fast_limited<Tag, FMT>(in[2 * j], ps, lim) |
+               (quant_word_fast_limited<Tag, FMT>(in[2 * j + 1], ps, lim) << 16);
+  } else {
+#pragma unroll
+    for (int j = 0; j < NW / 2; ++j)
+      out[j] = quant_word_slow<Tag, FMT>(in[2 * j], s) |
+               (quant_word_slow<Tag, FMT>(in[2 * j + 1], s) << 16);
+  }
+}
+
 // ---- FP32 inputs ---------------------------------------------------------------
 // Two FP8 codes (low byte from x0) of two fp32 inputs given as bit patterns,
 // for a finite scale: exact_quotient<2> on both lanes, -x by the sign bit.
@@ -141,6 +171,16 @@ __device__ __forceinline__ void quant_words_f32(const uint32_t* in, uint32_t* ou
       out[j] = quant_f32_pair_slow<FMT>(in[4 * j], in[4 * j + 1], s) |
                (quant_f32_pair_slow<FMT>(in[4 * j + 2], in[4 * j + 3], s) << 16);
   }
+}
+
+// quant_words_f32 with every input first clamped to [-lim, lim], NaN kept.
+template <int FMT, int NW>
+__device__ __forceinline__ void quant_words_f32_limited(const uint32_t* in, uint32_t* out, float s,
+                                                        float r, float lim) {
+  uint32_t c[NW];
+#pragma unroll
+  for (int j = 0; j < NW; ++j) c[j] = __float_as_uint(clamp_keep_nan(__uint_as_float(in[j]), lim));
+  quant_words_f32<FMT, NW>(c, out, s, r);
 }
 
 }  // namespace gs

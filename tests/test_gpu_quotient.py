@@ -49,8 +49,8 @@ def _near_midpoints(rng, s: np.ndarray, fmt: str, k: int = 3) -> np.ndarray:
     """fp32 x with x / s within a few ulps of an FP8 midpoint (random
     midpoint, random sign), one per entry of s."""
     m = _midpoints(fmt)[rng.integers(0, _midpoints(fmt).size, s.shape)]
-    base = (m * s.astype(np.float64)).astype(np.float32).view(np.int32)
-    x = (base + rng.integers(-k, k + 1, s.shape)).view(np.float32)
+    base = (m * s.astype(np.float64)).astype(np.float32).view(np.int32).astype(np.int64)
+    x = (base + rng.integers(-k, k + 1, s.shape)).astype(np.int32).view(np.float32)
     return np.where(rng.random(s.shape) < 0.5, -x, x).astype(np.float32)
 
 
