@@ -772,7 +772,7 @@ def run_sweep(args):
 
 # ---- one kernel alone --------------------------------------------------------------
 
-ONLY_CASES = ["unscale", "quant_1x128", "dequant", "quant_128x128", "quant_128x128_tma",
+ONLY_CASES = ["unscale", "quant_1x128", "dequant", "quant_128x128", "quant_128x128_16b",
               "quant_tensor", "quant_mx", "dequant_mx", "quant_delayed", "unscale_norm",
               "master_update", "gemm"]
 # the rows beyond the step, timed after it in the default run
@@ -859,10 +859,10 @@ def kernel_case(torch, gs, name: str) -> dict:
                 "flops": 2 * a.rows * w.rows * a.cols,
                 "workload": "E4M3 [16384, 8192] (1x128 scales) x [28672, 8192]^T (128x128 "
                             "scales) -> bf16", "keep": (qa, sa, qb, sb, d)}
-    if name in ("quant_128x128", "quant_128x128_tma"):
+    if name in ("quant_128x128", "quant_128x128_16b"):
         w = wl.cfg4_weight()
-        # the TMA-staged kernel takes inputs 16-byte but not 32-byte aligned
-        off = 8 if name == "quant_128x128_tma" else 0
+        # input 16-byte but not 32-byte aligned: the 16-byte-load kernel
+        off = 8 if name == "quant_128x128_16b" else 0
         xbuf = torch.empty(w.numel + off, dtype=torch.bfloat16, device=dev)
         x = xbuf[off:].view(w.rows, w.cols)
         dg.fill_device(w.spec, 0, w.numel, x.data_ptr(), st)

@@ -452,8 +452,7 @@ int fp8_quant_block(const void* x, int in_dtype, int64_t R, int64_t C, int32_t b
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = block_r == 1
                       ? launch_quant_1x128(x, in_dtype, R, C, fmt, q, scales, st)
-                      : launch_quant_128x128(x, in_dtype, R, C, fmt, q, scales,
-                                             device_status_ptr(), st);
+                      : launch_quant_128x128(x, in_dtype, R, C, fmt, q, scales, st);
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
 

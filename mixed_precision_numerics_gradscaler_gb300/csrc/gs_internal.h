@@ -52,11 +52,11 @@ cudaError_t launch_master_update_sgd(const MChunk* d_chunks, int64_t n_chunks, f
 cudaError_t launch_quant_1x128(const void* x, int dtype, int64_t R, int64_t C, int fmt, uint8_t* q,
                                float* scales, cudaStream_t stream);
 cudaError_t launch_quant_128x128(const void* x, int dtype, int64_t R, int64_t C, int fmt,
-                                 uint8_t* q, float* scales, int32_t* status,
-                                 cudaStream_t stream);
+                                 uint8_t* q, float* scales, cudaStream_t stream);
 // The 128x128 kernels behind launch_quant_128x128: direct 32-byte loads
 // (x 32-byte aligned; q 16-byte aligned for 16-bit input, 8-byte for FP32),
-// and one CTA per block for any dtype and alignment.
+// direct 16-byte loads (16-bit x 16-byte aligned, q 8-byte aligned), and one
+// CTA per block for any dtype and alignment.
 cudaError_t launch_quant_128x128_v8(const void* x, int dtype, int64_t R, int64_t C, int fmt,
                                     uint8_t* q, float* scales, cudaStream_t stream);
 cudaError_t launch_quant_128x128_simple(const void* x, int dtype, int64_t R, int64_t C, int fmt,

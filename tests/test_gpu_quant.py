@@ -83,7 +83,7 @@ def test_quant_128x128_shapes(gs, orc, fmt, dt, R, C):
     rng = np.random.default_rng(R * 3 + C)
     xh, xd = _host_input(rng, R, C, dt, special=True)
     _check_block(gs, orc, xh, xd, dt, 128, 128, fmt)
-    if dt != "f32":   # the same block with 8-byte-aligned codes (the TMA path)
+    if dt != "f32":   # the same block with 8-byte-aligned codes (the 16-byte-load path)
         _check_block(gs, orc, xh, xd, dt, 128, 128, fmt, q_off=8)
 
 
@@ -438,7 +438,7 @@ def test_exhaustive_fp32_cast_at_unit_scale(gs, orc, fmt):
 def test_block_quant_random_cases(gs, orc):
     """30 seeded random cases of the block quantiser and dequantiser: block
     shape, rows and columns, input type, format, special values, and input
-    and code buffers at random offsets (so the vector, TMA and scalar paths
+    and code buffers at random offsets (so the 32-byte, 16-byte and scalar paths
     all run) -- bit for bit against the oracle."""
     rng = np.random.default_rng(77)
     for i in range(30):
@@ -456,22 +456,22 @@ def test_block_quant_random_cases(gs, orc):
         _check_block(gs, orc, xh, xd, dt, br, 128, fmt, q_off=int(rng.choice([0, 1, 8, 16])))
 
 
-@pytest.mark.parametrize("path", ["direct", "tma"])
+@pytest.mark.parametrize("path", ["load32", "load16"])
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 def test_quant_128x128_several_blocks_per_cta(gs, orc, path, dt, fmt):
     """41 x 13 blocks of 128x128: more blocks than either 128x128 kernel
     launches CTAs (two per SM), with a column count that does not
     divide the grid, so CTAs walk several blocks and their block coordinates
-    wrap rows -- through the direct-load kernel (32-byte aligned input) and
-    the TMA-staged one (input at a 16-byte offset; FP32 input there takes
+    wrap rows -- through the 32-byte-load kernel (32-byte aligned input) and
+    the 16-byte-load one (input at a 16-byte offset; FP32 input there takes
     the one-CTA-per-block kernel); block (0, 0) holds NaN, +-Inf, zeros and
     tiny values. Bit for bit against the oracle."""
-    rng = np.random.default_rng(1000 + 100 * (path == "tma") + 10 * ["bf16", "f16", "f32"].index(dt)
-                                + (fmt == "e5m2"))
+    rng = np.random.default_rng(1000 + 100 * (path == "load16") +
+                                10 * ["bf16", "f16", "f32"].index(dt) + (fmt == "e5m2"))
     R, C = 128 * 41, 128 * 13
     xh, xd = _host_input(rng, R, C, dt, special=True)
-    if path == "tma":
+    if path == "load16":
         off = 16 // xd.element_size()  # 16 bytes
         big = torch.zeros(R * C + off, dtype=xd.dtype, device=DEV)
         big[off:] = xd.reshape(-1)
