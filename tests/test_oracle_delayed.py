@@ -32,6 +32,28 @@ def test_delayed_first_step_with_empty_history_saturates(orc):
     assert q.tolist() == [0x7E, 0xFE, 0x7E, 0x00, 0x80]
 
 
+@pytest.mark.parametrize("fmt,mx_code", [(E4M3, 0x7E), (E5M2, 0x7B)])
+def test_delayed_quotient_beyond_fp32_saturates(orc, fmt, mx_code):
+    """The scale comes from the history, not from x, so x / s can exceed the
+    fp32 range or be infinite: the IEEE quotient is then +-Inf, and the
+    pages' clamp to +-MAX before the cast makes the code +-MAX; a NaN stays
+    the NaN code.  The same elements as bf16 and fp16 inputs (fp16 holds
+    only the infinities and the small values) give the same codes."""
+    x = np.array([3.0e38, -3.0e38, np.inf, -np.inf, np.nan, 1e-3, 0.0], np.float32)
+    d = orc.DelayedScaling(2, history=[1e-10, 2e-11])
+    q, s = d.quant(x, fmt)
+    assert s == np.float32(np.float32(1e-10) / np.float32(orc.fp8_max(fmt)))
+    assert np.isinf(np.float32(3.0e38) / s)          # the quotient overflows fp32
+    sat, nsat = mx_code, mx_code | 0x80
+    assert q.tolist() == [sat, nsat, sat, nsat, 0x7F, sat, 0x00]
+    qb, _ = orc.DelayedScaling(2, history=[1e-10, 2e-11]).quant(
+        orc.encode_array(x.astype(np.float64), orc.BF16), fmt, dtype=orc.BF16)
+    assert qb.tolist() == q.tolist()
+    h = np.array([0x7C00, 0xFC00, 0x7E00, 0x0000, 0x8000], np.uint16)   # fp16 +-Inf, NaN, +-0
+    qh, _ = orc.DelayedScaling(2, history=[1e-10, 2e-11]).quant(h, fmt, dtype=orc.F16)
+    assert qh.tolist() == [sat, nsat, 0x7F, 0x00, 0x80]
+
+
 def test_delayed_spike_uses_the_past_then_dominates_for_the_window(orc):
     """The scale applied on a step comes from earlier steps: a spike is
     saturated on its own step, then sets the scale for exactly H steps."""
