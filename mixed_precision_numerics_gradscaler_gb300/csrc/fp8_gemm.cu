@@ -72,7 +72,11 @@ constexpr int kGTmemCols = 2 * kGBN;       // two 256-column fp32 accumulators
 constexpr int kGOutBytes = 32 * 128;      // per promotion warp: 32 rows x 128 bytes of D
 constexpr int kGSmemBytes = kGStages * kGStageBytes + kGEpiWarps * kGOutBytes + 1024 + 256;
 static_assert(kGSmemBytes <= 232448, "dynamic shared memory above the per-CTA limit");
-constexpr int kGroupM = 16;                // tile rows per raster group
+// Tile rows per raster group: B is read from DRAM once per group.  Measured
+// on GB300 (16384 x 28672 x 8192): 16 rows read 2.02 GB per launch, 32 rows
+// 1.19 GB at the same or a slightly higher rate, 40, 48 and 64 rows 1.64,
+// 2.03 and 3.55 GB (the A panel of a group stops fitting in L2).
+constexpr int kGroupM = 32;
 constexpr uint64_t kGWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t g_smem_u32(const void* p) {
