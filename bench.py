@@ -65,7 +65,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--sweep", action="store_true", help="bandwidth sweep 1 MiB..8 GiB (config 5)")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=6)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--only", choices=ONLY_CASES,
                    help="time one kernel alone on a small case (for ncu captures)")
@@ -259,8 +259,11 @@ class Workload:
         st = torch.cuda.current_stream().cuda_stream
         self.cfg2 = wl.cfg2_grads()
         f16, f32, bf16, u8 = torch.float16, torch.float32, torch.bfloat16, torch.uint8
-        self.grads = [torch.empty(n, dtype=f16, device=dev) for n in self.cfg2.numels]
-        self.outs = [torch.empty(n, dtype=f32, device=dev) for n in self.cfg2.numels]
+        # the gradient list and its outputs as views into two flat buffers (one
+        # host<->device copy each in the end-to-end loop)
+        self.g_flat = torch.empty(self.cfg2.total, dtype=f16, device=dev)
+        self.o_flat = torch.empty(self.cfg2.total, dtype=f32, device=dev)
+        self.grads, self.outs = self._views(self.g_flat, self.o_flat)
         for t, (g, n) in enumerate(zip(self.grads, self.cfg2.numels)):
             dg.fill_device(self.cfg2.spec(t, 0), 0, n, g.data_ptr(), st)
         self.tl = gs.gs_tensor_list_create(self.grads, self.outs)
@@ -299,6 +302,16 @@ class Workload:
         self.launches = {"unscale_check_update": 1, "quant_1x128": 1, "dequant_1x128_bf16": 1,
                          "quant_128x128": 1, "quant_tensor_e5m2": 2}
         torch.cuda.synchronize()
+
+    def _views(self, g_flat, o_flat):
+        """Per-tensor views of the flat gradient and output buffers (every
+        tensor starts at a multiple of 4096 elements)."""
+        grads, outs, off = [], [], 0
+        for n in self.cfg2.numels:
+            grads.append(g_flat[off:off + n])
+            outs.append(o_flat[off:off + n])
+            off += n
+        return grads, outs
 
     @property
     def bytes_per_step(self) -> int:
@@ -339,7 +352,10 @@ class Workload:
     # inputs go up (copy-in stream) while step k computes and step k-1's
     # results come down (copy-out stream).  Two device buffer sets (two
     # gradient lists) alternate; events keep every buffer from being
-    # overwritten while a copy or a kernel still uses it.
+    # overwritten while a copy or a kernel still uses it.  Each gradient list
+    # and its outputs live in one flat buffer, so a step is 4 copies up and
+    # 11 down: hundreds of per-tensor copies filled the driver's command
+    # queue and stalled the host thread that issues the next step.
     def e2e_setup(self):
         torch, gs = self.torch, self.gs
         pin = dict(pin_memory=True)
@@ -347,20 +363,20 @@ class Workload:
         self.sets = []
         for k in range(2):
             if k == 0:
-                d = dict(grads=self.grads, outs=self.outs, x3=self.x3, q3=self.q3, s3=self.s3,
-                         y3=self.y3, x4=self.x4, q4=self.q4, s4=self.s4, x5=self.x5, q5=self.q5,
-                         s5=self.s5, tl=self.tl)
+                d = dict(g_flat=self.g_flat, o_flat=self.o_flat, grads=self.grads, outs=self.outs,
+                         x3=self.x3, q3=self.q3, s3=self.s3, y3=self.y3, x4=self.x4, q4=self.q4,
+                         s4=self.s4, x5=self.x5, q5=self.q5, s5=self.s5, tl=self.tl)
             else:
-                d = dict(grads=[torch.empty_like(g) for g in self.grads],
-                         outs=[torch.empty_like(o) for o in self.outs],
+                d = dict(g_flat=torch.empty_like(self.g_flat), o_flat=torch.empty_like(self.o_flat),
                          x3=torch.empty_like(self.x3), q3=torch.empty_like(self.q3),
                          s3=torch.empty_like(self.s3), y3=torch.empty_like(self.y3),
                          x4=torch.empty_like(self.x4), q4=torch.empty_like(self.q4),
                          s4=torch.empty_like(self.s4), x5=torch.empty_like(self.x5),
                          q5=torch.empty_like(self.q5), s5=torch.empty_like(self.s5))
+                d["grads"], d["outs"] = self._views(d["g_flat"], d["o_flat"])
                 d["tl"] = gs.gs_tensor_list_create(d["grads"], d["outs"])
-            d["ins"] = d["grads"] + [d["x3"], d["x4"], d["x5"]]
-            d["res"] = d["outs"] + [d["q3"], d["s3"], d["y3"], d["q4"], d["s4"], d["q5"], d["s5"]]
+            d["ins"] = [d["g_flat"], d["x3"], d["x4"], d["x5"]]
+            d["res"] = [d["o_flat"], d["q3"], d["s3"], d["y3"], d["q4"], d["s4"], d["q5"], d["s5"]]
             self.sets.append(d)
         self.h_in = [torch.empty(t.shape, dtype=t.dtype, **pin) for t in self.sets[0]["ins"]]
         for h, t in zip(self.h_in, self.sets[0]["ins"]):
@@ -387,7 +403,7 @@ class Workload:
         self.tl.close()
         self.sets = []
         self.h_in = self.h_out = None
-        self.grads = self.outs = None
+        self.grads = self.outs = self.g_flat = self.o_flat = None
         self.x3 = self.q3 = self.s3 = self.y3 = self.x4 = self.q4 = self.s4 = None
         self.x5 = self.q5 = self.s5 = self.ws = None
 
