@@ -354,8 +354,7 @@ class Workload:
     # gradient lists) alternate; events keep every buffer from being
     # overwritten while a copy or a kernel still uses it.  Each gradient list
     # and its outputs live in one flat buffer, so a step is 4 copies up and
-    # 11 down: hundreds of per-tensor copies filled the driver's command
-    # queue and stalled the host thread that issues the next step.
+    # 11 down.
     def e2e_setup(self):
         torch, gs = self.torch, self.gs
         pin = dict(pin_memory=True)
