@@ -153,11 +153,10 @@ def measure_link(torch, nbytes: int = 1 << 30, reps: int = 3) -> dict:
 
 # ---- peaks, traffic, clocks --------------------------------------------------------
 
-def fp8_peak(timed_s: float) -> tuple[float, str]:
+def fp8_peak(sustained: bool) -> tuple[float, str]:
     """Dense FP8 tensor peak: a measured bf16 GEMM rate x 2 (the nominal
-    FP8 / bf16 ratio of the part) -- the sustained (power-capped) rate when
-    the timed loop runs for half a second or more, else the burst rate."""
-    sustained = timed_s >= 0.5
+    FP8 / bf16 ratio of the part) -- the sustained (power-capped) rate for a
+    loop that runs for half a second or more, else the burst rate."""
     try:
         with open(PEAKS_FILE) as f:
             pk = json.load(f)
@@ -930,8 +929,8 @@ def time_case(torch, case: dict, warmup: int, iters: int, reps: int = 10) -> dic
            "launches_timed": iters * reps, "timed_s": round(sum(ts) * reps / 1e3, 3),
            "clocks": clocks.summary()}
     if "flops" in case:
-        peak_s, src_s = fp8_peak(1.0)
-        peak_b, src_b = fp8_peak(0.0)
+        peak_s, src_s = fp8_peak(sustained=True)
+        peak_b, src_b = fp8_peak(sustained=False)
         tf = case["flops"] / ms / 1e9
         first = case["flops"] / ts[0] / 1e9
         out.update({"flops": case["flops"], "tflops": round(tf, 1), "peak_tflops": peak_s,

@@ -31,14 +31,14 @@ def test_clock_summary_uses_loaded_samples_and_reports_throttle_reasons():
     assert _sampler([idle])["samples"] == 1
 
 
-def test_fp8_peak_is_sustained_for_long_loops(tmp_path, monkeypatch):
+def test_fp8_peak_burst_and_sustained(tmp_path, monkeypatch):
     peaks = tmp_path / "peaks.json"
     peaks.write_text(json.dumps({"bf16_tflops": 1932.5, "bf16_tflops_sustained": 1759.5}))
     monkeypatch.setattr(bench, "PEAKS_FILE", str(peaks))
-    assert bench.fp8_peak(0.1) == (3865.0, "measured bf16_tflops x 2")
-    assert bench.fp8_peak(2.0) == (3519.0, "measured bf16_tflops_sustained x 2")
+    assert bench.fp8_peak(sustained=False) == (3865.0, "measured bf16_tflops x 2")
+    assert bench.fp8_peak(sustained=True) == (3519.0, "measured bf16_tflops_sustained x 2")
     monkeypatch.setattr(bench, "PEAKS_FILE", str(tmp_path / "absent.json"))
-    assert bench.fp8_peak(0.1)[1].startswith("fallback")
+    assert bench.fp8_peak(sustained=False)[1].startswith("fallback")
 
 
 def test_recorded_traffic_is_dropped_when_the_kernel_sources_change(tmp_path, monkeypatch):
