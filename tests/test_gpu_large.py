@@ -1,7 +1,8 @@
-"""The 128x128 and per-tensor quantisers on single tensors past 2^32
-elements (8 GiB of bf16 input), against the oracle ("Mixed precision and FP8
-training", section "FP8 training": per_block and per_tensor; "Why FP8
-training is stable", "Failure 1": one scale for the whole tensor).  Element
+"""The 128x128, per-tensor, MXFP8 and delayed-scaling quantisers on single
+tensors past 2^32 elements (8 GiB of bf16 input), against the oracle ("Mixed
+precision and FP8 training", section "FP8 training": per_block, per_tensor,
+and the MX formats' one scale per 32 elements; "Why FP8 training is stable",
+"Failure 1": one scale for the whole tensor, or one from a history).  Element
 indices pass 2^31 and 2^32 and byte offsets 2^32 and 2^33 there; the inputs
 have config 4's distributions, generated on the device and regenerated on
 the host for the oracle."""
@@ -88,5 +89,91 @@ def test_quant_tensor_past_2_32_elements(gs, orc):
                      for v in orc.decode_array(xs, orc.BF16)], np.uint8)
     got = q[torch.from_numpy(pos).to(DEV)].cpu().numpy()
     assert_same_bytes(got, want, "per-tensor codes at sampled positions")
+    del q
+    torch.cuda.empty_cache()
+
+
+def test_quant_mx_past_2_32_elements(gs, orc):
+    """MXFP8 E4M3 (1x32 blocks, E8M0 scales) of bf16 [524291, 8192] with
+    config 3's distribution: every code and every scale byte against the
+    oracle over slabs on every host core; the bf16 dequantisation at sampled
+    blocks around element 2^31, 2^32, the end and 10^5 random positions."""
+    R = (1 << 19) + 3
+    a = wl.cfg5_act(R * 8192 * 2)
+    C = a.cols
+    n = R * C
+    x = torch.empty(R, C, dtype=torch.bfloat16, device=DEV)
+    dg.fill_device(a.spec, 0, n, x.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    q = torch.empty(R, C, dtype=torch.uint8, device=DEV)
+    s = torch.empty(R, C // 32, dtype=torch.uint8, device=DEV)
+    gs.fp8_quant_mx(x, "e4m3", q, s)
+    del x
+    y = torch.empty(R, C, dtype=torch.bfloat16, device=DEV)
+    gs.fp8_dequant_mx(q, s, "e4m3", y)
+    torch.cuda.synchronize()
+    q_h, s_h = q.cpu().numpy(), s.cpu().numpy()
+    del q, s
+
+    slab = 256
+
+    def check(r0):
+        r1 = min(R, r0 + slab)
+        xb = dg.fill_host(a.spec, r0 * C, (r1 - r0) * C).reshape(r1 - r0, C)
+        rq, rs = orc.quant_mx(xb, orc.E4M3, dtype=orc.BF16)
+        return r0, int(np.count_nonzero(rq != q_h[r0:r1])), int(np.count_nonzero(rs != s_h[r0:r1]))
+
+    bad = [r for r in pmap(check, range(0, R, slab)) if r[1] or r[2]]
+    assert not bad, f"rows from {bad[:3]} (row, bad codes, bad scales) differ from the oracle"
+
+    rng = np.random.default_rng(321)
+    pos = np.concatenate([rng.integers(0, n, 100_000),
+                          *[np.arange(c - 2048, min(n, c + 2048)) for c in (1 << 31, 1 << 32, n - 2048)]])
+    blocks = np.unique(pos // 32)
+    idx = (blocks[:, None] * 32 + np.arange(32)[None, :]).reshape(-1)
+    ry = orc.dequant_mx(q_h.reshape(-1)[idx].reshape(-1, 32), s_h.reshape(-1)[blocks].reshape(-1, 1),
+                        orc.E4M3, out_dtype=orc.BF16)
+    got = y.view(-1)[torch.from_numpy(idx).to(DEV)].view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (got == ry.reshape(-1)).all(), "MX dequantised bf16 differs from the oracle"
+    del y
+    torch.cuda.empty_cache()
+
+
+def test_quant_delayed_past_2_32_elements(gs, orc):
+    """Delayed E5M2 scaling of one bf16 tensor of 2^32 + 4099 elements with
+    config 4's gradient distribution under a seeded history: the scale used
+    is the oracle's from the history, the codes match the oracle's quantiser
+    at sampled positions, and the amax written into the ring is the oracle's
+    amax of the whole tensor."""
+    n = (1 << 32) + 4099
+    spec = wl.cfg4_grad().spec
+    x = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    dg.fill_device(spec, 0, n, x.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    q = torch.empty(n, dtype=torch.uint8, device=DEV)
+    hist_h = np.array([3e-3, 7.5e-3, 1e-4, 0.0], np.float32)
+    hist = torch.from_numpy(hist_h.copy()).to(DEV)
+    pos_d = torch.tensor([2], dtype=torch.int32, device=DEV)
+    used = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=DEV)
+    gs.fp8_quant_tensor_delayed(x, "e5m2", q, hist, pos_d, used, ws)
+    del x
+    torch.cuda.synchronize()
+    scale = np.float32(orc.scale_from_amax(float(hist_h.max()), orc.E5M2))
+    assert_same_f32(used.cpu().numpy(), np.array([scale], np.float32), "scale used")
+    slab = 1 << 24
+    amax = max(pmap(lambda i: orc.amax(dg.fill_host(spec, i, min(slab, n - i)), dtype=orc.BF16),
+                    range(0, n, slab)))
+    want_hist = hist_h.copy()
+    want_hist[2] = np.float32(amax)
+    assert_same_f32(hist.cpu().numpy(), want_hist, "history after the step")
+    assert int(pos_d.item()) == 3
+    rng = np.random.default_rng(456)
+    pos = np.unique(np.concatenate([
+        rng.integers(0, n, 100_000),
+        *[np.arange(c - 2048, min(n, c + 2048)) for c in (1 << 31, 1 << 32, n - 2048)]]))
+    xs = dg.fill_host_idx(spec, pos)
+    want = np.array([orc.quant_one(float(v), float(scale), orc.E5M2)
+                     for v in orc.decode_array(xs, orc.BF16)], np.uint8)
+    got = q[torch.from_numpy(pos).to(DEV)].cpu().numpy()
+    assert_same_bytes(got, want, "delayed codes at sampled positions")
     del q
     torch.cuda.empty_cache()
