@@ -370,8 +370,8 @@ def fp8_gemm_block_scaled(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, 
 
 
 def gs_test_set_stall(on: bool) -> None:
-    """Test hook: the TMA-fed kernels issue no loads while on, so their
-    bounded waits run out and they report GS_ERR_TIMEOUT."""
+    """Test hook: the block-scaled FP8 GEMM issues no TMA loads while on, so
+    its bounded waits run out and it reports GS_ERR_TIMEOUT."""
     _check(_lib.gs_test_set_stall(1 if on else 0), "gs_test_set_stall")
 
 

@@ -34,8 +34,8 @@ struct Span {
 // O((writes + reads) log writes).
 bool spans_conflict(Span* writes, size_t n_writes, const Span* reads, size_t n_reads);
 
-// Test hook (gs_test_set_stall): nonzero makes the TMA-fed kernels issue no
-// loads, so that their bounded waits run out.
+// Test hook (gs_test_set_stall): nonzero makes the block-scaled FP8 GEMM issue
+// no TMA loads, so that its bounded waits run out.
 int test_stall();
 
 // Launchers.  Each returns the launch's cudaError_t.
