@@ -575,18 +575,20 @@ def run_reference(args):
     sample = OracleSample()
     sample.run()  # loads the oracle library before any thread starts
     n = _oracle_threads()
-    oracle_parallel(sample, n, reps=args.warmup)
-    runs, el = oracle_parallel(sample, n, reps=args.steps)
+    # one step = one sample on every host thread, so each step uses all n
+    oracle_parallel(sample, n, reps=args.warmup * n)
+    runs, el = oracle_parallel(sample, n, reps=args.steps * n)
     value = throughput(sample.bytes * runs, el)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": WORKLOAD, "reference": "CPU oracle (plain C, scalar), the "
-                       "pages ship no implementation; steps spread over the host threads",
-                       "sample_bytes_per_step": sample.bytes},
+                       "pages ship no implementation; each step runs the sample once on "
+                       "every host thread", "sample_bytes_per_step": sample.bytes * n},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle",
-                             "cpu_model": cpu_model(), "sample": sample.desc},
+                             "cpu_model": cpu_model(),
+                             "sample": f"{sample.desc}, once per thread on {n} threads per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

@@ -96,6 +96,9 @@ def test_reference_arm_prints_one_complete_line(monkeypatch, capsys):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert cb["sample"] and cb["cpu_model"]
+    # every step runs one sample on each of the threads it reports
+    assert cb["cores"] == bench._oracle_threads()
+    assert d["config"]["sample_bytes_per_step"] == bench.OracleSample().bytes * cb["cores"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
 
