@@ -15,7 +15,8 @@ HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 def _declared_functions():
     names = set()
     for h in HEADERS:
-        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        with open(h) as f:
+            src = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
         names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", src, flags=re.M))
     return sorted(names)
 

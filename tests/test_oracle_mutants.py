@@ -106,9 +106,11 @@ def _build_variant(tmp, name, patch):
     if patch is not None:
         fname, old, new = patch
         path = os.path.join(d, fname)
-        src = open(path).read()
+        with open(path) as f:
+            src = f.read()
         assert src.count(old) == 1, f"mutation anchor not unique/found: {old!r}"
-        open(path, "w").write(src.replace(old, new))
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
     lib = os.path.join(d, "liboracle.so")
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
                     "-shared", "-o", lib, *[os.path.join(d, f) for f in
