@@ -16,7 +16,10 @@
  *     library failed (see gs_last_cuda_error).  Nothing throws or aborts.
  *   - Streams: `stream` is a cudaStream_t passed as void*; NULL is the
  *     legacy default stream.  Every compute call is asynchronous on that
- *     stream and never synchronises the host.
+ *     stream and never synchronises the host.  The handle is passed to CUDA
+ *     as given: it must be a live stream of the current context (CUDA has
+ *     no safe check for an arbitrary handle; a launch CUDA refuses returns
+ *     GS_ERR_CUDA).
  *   - Memory: every data pointer is device memory of the current device
  *     (or managed memory, or mapped host memory whose device address equals
  *     its host address); pointers the device cannot use as given are
