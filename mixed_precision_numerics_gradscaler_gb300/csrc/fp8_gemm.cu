@@ -557,7 +557,7 @@ static cudaError_t gemm_t(const CUtensorMap& ma, const CUtensorMap& mb, const CU
       regs_err = cudaErrorInvalidConfiguration;
   });
   if (regs_err != cudaSuccess) return regs_err;
-  int occ = 0;  // also raises the shared-memory limit on this device
+  int occ = 0;  // also raises the shared-memory limit in this context
   const cudaError_t e = kernel_blocks_per_sm((const void*)k, kGThreads, kGSmemBytes, &occ);
   if (e != cudaSuccess) return e;
   if (occ < 1) return cudaErrorInvalidConfiguration;

@@ -1,6 +1,7 @@
 // gs_api.cu -- the C ABI declared in include/gsfp8.h: argument validation
 // on the host (nothing is launched unless every check passes), the
 // gradient-list chunk table, status codes and launch dispatch.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -18,7 +19,7 @@
 #include "gsfp8.h"
 #include "gsfp8_test.h"
 
-// The device status word (GS_OK or GS_ERR_TIMEOUT), one per device.
+// The device status word (GS_OK or GS_ERR_TIMEOUT), one per CUDA context.
 __device__ int32_t g_gs_device_status = 0;
 
 struct gs_tensor_list {
@@ -61,10 +62,85 @@ int sm_count() {
   return n;
 }
 
+// The driver's context queries, reached through the runtime (the library
+// links no driver library).  Looked up once per process.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+struct CtxQueries {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+static const CtxQueries& ctx_queries() {
+  static CtxQueries q;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r) ==
+            cudaSuccess && r == cudaDriverEntryPointSuccess)
+      q.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &r) ==
+            cudaSuccess && r == cudaDriverEntryPointSuccess)
+      q.get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  return q;
+}
+
+bool current_context_id(unsigned long long* id) {
+  const CtxQueries& q = ctx_queries();
+  CUcontext ctx = nullptr;
+  *id = 0;
+  if (!q.get_current || !q.get_id || q.get_current(&ctx) != CUDA_SUCCESS) return false;
+  return ctx == nullptr || q.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// ID of the current context, making the device's primary context current
+// first when no context is (as the runtime does on its first call).
+static cudaError_t context_id(unsigned long long* id) {
+  if (!current_context_id(id)) return cudaErrorDeviceUninitialized;
+  if (*id != 0) return cudaSuccess;
+  const cudaError_t e = cudaFree(nullptr);  // initialises the primary context, frees nothing
+  if (e != cudaSuccess) return e;
+  return current_context_id(id) && *id != 0 ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+cudaError_t symbol_address(const void* symbol, void** out) {
+  constexpr int kSlots = 64;
+  struct Slot {
+    const void* symbol;
+    unsigned long long ctx_id;
+    void* ptr;
+  };
+  static Slot slots[kSlots] = {};
+  static int next_slot = 0;
+  static std::mutex mu;
+  *out = nullptr;
+  unsigned long long id = 0;
+  cudaError_t e = context_id(&id);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Slot& sl : slots)
+    if (sl.ctx_id == id && sl.symbol == symbol) {
+      *out = sl.ptr;
+      return cudaSuccess;
+    }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, symbol);
+  if (e != cudaSuccess) return e;
+  slots[next_slot] = Slot{symbol, id, p};
+  next_slot = (next_slot + 1) % kSlots;
+  *out = p;
+  return cudaSuccess;
+}
+
 cudaError_t kernel_blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* blocks) {
   static std::mutex mu;
-  static std::map<std::tuple<const void*, int, int, int>, int> cache;
-  const auto key = std::make_tuple(kernel, current_device(), threads, smem_bytes);
+  static std::map<std::tuple<const void*, unsigned long long, int, int>, int> cache;
+  unsigned long long ctx = 0;
+  const cudaError_t ce = context_id(&ctx);
+  if (ce != cudaSuccess) return ce;
+  const auto key = std::make_tuple(kernel, ctx, threads, smem_bytes);
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it == cache.end()) {
@@ -84,18 +160,12 @@ cudaError_t kernel_blocks_per_sm(const void* kernel, int threads, int smem_bytes
 
 void record_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }
 
-static int32_t* device_status_ptr() {
-  static int32_t* cache[kMaxDevices] = {nullptr};
-  static std::mutex mu;
-  const int d = current_device();
-  if (d < 0 || d >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[d]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_gs_device_status) != cudaSuccess) return nullptr;
-    cache[d] = static_cast<int32_t*>(p);
-  }
-  return cache[d];
+// The status word's address in the current context.
+static cudaError_t device_status_ptr(int32_t** out) {
+  void* p = nullptr;
+  const cudaError_t e = symbol_address((const void*)&g_gs_device_status, &p);
+  *out = static_cast<int32_t*>(p);
+  return e;
 }
 
 static int cuda_fail(cudaError_t e) {
@@ -584,9 +654,10 @@ int fp8_gemm_block_scaled(const uint8_t* qa, const float* sa, const uint8_t* qb,
         overlaps(d, nd, sb, nsb))
       return GS_ERR_ARG;
   }
-  int32_t* status = device_status_ptr();
-  if (!status) return cuda_fail(cudaGetLastError());
-  cudaError_t e = launch_gemm_fp8_block_scaled(qa, sa, qb, sb, M, N, K, fmt_a, fmt_b, out_dtype, d,
+  int32_t* status = nullptr;
+  cudaError_t e = device_status_ptr(&status);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_gemm_fp8_block_scaled(qa, sa, qb, sb, M, N, K, fmt_a, fmt_b, out_dtype, d,
                                                status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GS_OK : cuda_fail(e);
 }
@@ -598,10 +669,11 @@ int gs_test_set_stall(int on) {
 
 int gs_device_status(int32_t* h_status, void* stream) {
   if (!h_status) return GS_ERR_NULL;
-  int32_t* p = device_status_ptr();
-  if (!p) return cuda_fail(cudaGetLastError());
+  int32_t* p = nullptr;
+  cudaError_t e = device_status_ptr(&p);
+  if (e != cudaSuccess) return cuda_fail(e);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(h_status, p, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  e = cudaMemcpyAsync(h_status, p, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int32_t), st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return e == cudaSuccess ? GS_OK : cuda_fail(e);

@@ -12,12 +12,28 @@ namespace gs {
 // Cached device properties of the current device.
 int sm_count();
 
-// Resident blocks per SM of `kernel` at (threads, dynamic smem bytes) on the
-// current device; the first call per kernel and device also raises the
-// kernel's dynamic shared-memory limit there (function attributes are per
-// device).  Thread-safe; cached.
+// Resident blocks per SM of `kernel` at (threads, dynamic smem bytes) in the
+// CUDA context current on this thread; the first call per kernel and context
+// also raises the kernel's dynamic shared-memory limit there (function
+// attributes belong to the module loaded in a context, so a new primary
+// context after cudaDeviceReset needs them again).  Thread-safe; cached
+// under the context's ID.
 cudaError_t kernel_blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* blocks);
 int current_device();
+
+// ID of the CUDA context current on this thread (0 and true when none is
+// current yet; false when the driver cannot be queried).  The driver never
+// hands out an ID twice in a process, whereas a new context may reuse a
+// destroyed one's handle, so caches of per-context state use the ID as key.
+bool current_context_id(unsigned long long* id);
+
+// Device address of the module global `symbol` (a __device__ variable of
+// this library) in the CUDA context current on this thread.  Every context
+// that loads the library holds its own copy of each global at its own
+// address, so the address is looked up with cudaGetSymbolAddress on the
+// first call in a context and cached under the context's ID (a fixed table,
+// no heap allocation).  Thread-safe.
+cudaError_t symbol_address(const void* symbol, void** out);
 
 // Records e as the calling thread's last CUDA error (gs_last_cuda_error).
 void record_cuda_error(cudaError_t e);

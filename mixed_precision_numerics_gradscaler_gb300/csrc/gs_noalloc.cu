@@ -14,13 +14,11 @@
 // a one-CTA kernel expands it into chunks inside the array and clears the
 // epilogue words; then the same unscale/check/update kernel as
 // gs_unscale_check_update runs on it.
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
 
 #include <cmath>
-#include <mutex>
 
 #include "gs_internal.h"
 #include "gsfp8.h"
@@ -57,88 +55,6 @@ __global__ void noalloc_build_chunks(const __grid_constant__ TensorTable tt, uns
     for (int64_t c = threadIdx.x; c < nc; c += blockDim.x)
       chunks[tt.first_chunk[t] + c] = chunk_at(tt.in[t], tt.out[t], n, head, c);
   }
-}
-
-// The driver's context queries, reached through the runtime (the library
-// links no driver library).  Looked up once per process.
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-struct CtxQueries {
-  CtxGetCurrentFn get_current = nullptr;
-  CtxGetIdFn get_id = nullptr;
-};
-static const CtxQueries& ctx_queries() {
-  static CtxQueries q;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult r;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r) ==
-            cudaSuccess && r == cudaDriverEntryPointSuccess)
-      q.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
-    p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &r) ==
-            cudaSuccess && r == cudaDriverEntryPointSuccess)
-      q.get_id = reinterpret_cast<CtxGetIdFn>(p);
-  });
-  return q;
-}
-
-// ID of the CUDA context current on this thread, or 0 when there is none.
-// The driver never hands out an ID twice in a process, whereas a new
-// context may reuse a destroyed one's handle, so the ID is the key.
-static bool current_context_id(unsigned long long* id) {
-  const CtxQueries& q = ctx_queries();
-  CUcontext ctx = nullptr;
-  *id = 0;
-  if (!q.get_current || !q.get_id || q.get_current(&ctx) != CUDA_SUCCESS) return false;
-  return ctx == nullptr || q.get_id(ctx, id) == CUDA_SUCCESS;
-}
-
-// Device address of the scratch array in the CUDA context current on this
-// thread.  The array is a module global, so every context that loads the
-// library (each device's primary context, the new primary context that
-// follows a cudaDeviceReset, any context the caller creates) holds its own
-// copy at its own address.  The address is looked up with
-// cudaGetSymbolAddress on the first call in a context and cached under the
-// context's ID; a call in another context never sees it.
-static unsigned char* scratch_address(cudaError_t* err) {
-  constexpr int kSlots = 32;
-  struct Slot {
-    unsigned long long ctx_id;
-    unsigned char* ptr;
-  };
-  static Slot slots[kSlots] = {};
-  static int next_slot = 0;
-  static std::mutex mu;
-  unsigned long long id = 0;
-  if (!current_context_id(&id)) {
-    *err = cudaErrorDeviceUninitialized;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (id != 0)
-    for (const Slot& s : slots)
-      if (s.ctx_id == id) {
-        *err = cudaSuccess;
-        return s.ptr;
-      }
-  // First call in this context (or no context current yet: the lookup makes
-  // the device's primary context current, and its ID is read afterwards).
-  void* p = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-  if (e != cudaSuccess) {
-    *err = e;
-    return nullptr;
-  }
-  if (id == 0 && (!current_context_id(&id) || id == 0)) {
-    *err = cudaErrorDeviceUninitialized;
-    return nullptr;
-  }
-  slots[next_slot] = Slot{id, static_cast<unsigned char*>(p)};
-  next_slot = (next_slot + 1) % kSlots;
-  *err = cudaSuccess;
-  return static_cast<unsigned char*>(p);
 }
 
 }  // namespace gs
@@ -203,12 +119,17 @@ extern "C" int gs_unscale_check_update_noalloc(const void* const* grads, void* c
   for (const void* p : {(const void*)scale, (const void*)growth_tracker, (const void*)found_inf,
                         (const void*)skipped})
     if (p && !device_reachable(p)) return GS_ERR_ARG;
-  cudaError_t e = cudaSuccess;
-  unsigned char* scratch = scratch_address(&e);
-  if (!scratch) {
+  // The array's address in the current context: each context that loads
+  // the library (each device's primary context, the new primary context
+  // after cudaDeviceReset, any context the caller creates) holds its own
+  // copy, so the address is looked up per context (symbol_address).
+  void* scratch_p = nullptr;
+  cudaError_t e = symbol_address((const void*)g_noalloc_scratch, &scratch_p);
+  if (e != cudaSuccess) {
     record_cuda_error(e);
     return GS_ERR_CUDA;
   }
+  unsigned char* scratch = static_cast<unsigned char*>(scratch_p);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   noalloc_build_chunks<<<1, 256, 0, st>>>(tt, scratch);
   e = cudaGetLastError();
