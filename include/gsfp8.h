@@ -25,7 +25,8 @@
  *     its host address); pointers the device cannot use as given are
  *     rejected with GS_ERR_ARG.  The caller owns all
  *     data buffers.  The library allocates only inside
- *     gs_tensor_list_create; no compute call allocates.
+ *     gs_tensor_list_create and gs_param_list_create; no compute call
+ *     allocates.
  *   - Layout: row-major and contiguous; element [r, c] of an R x C array is
  *     at offset r * C + c.  Outputs must not overlap inputs.  Any element-
  *     aligned address is accepted; 16-byte-aligned buffers take the
@@ -91,9 +92,11 @@ typedef struct gs_tensor_list gs_tensor_list;
  *   outs[i]   -- device pointer to numels[i] FP32 values (written by
  *                gs_unscale_check_update)
  *   numels[i] -- >= 0; n_tensors >= 0 (0 gives an empty list)
- * Allocates device memory and copies the chunk table synchronously (the
- * only allocating call of this library).  The pointers are captured: the
- * list stays valid while those buffers live.  On error *out is NULL. */
+ * Allocates device memory, uploads the chunk table and clears the
+ * workspace, and returns once both are on the device (it synchronises the
+ * legacy default stream), so the first step may follow on any stream.  The
+ * pointers are captured: the list stays valid while those buffers live.  On
+ * error *out is NULL. */
 int gs_tensor_list_create(const void* const* grads, void* const* outs, const int64_t* numels,
                           int32_t n_tensors, gs_tensor_list** out);
 
@@ -166,7 +169,8 @@ int gs_unscale_check_update_hysteresis(const gs_tensor_list* list, float* scale,
 /* Opaque list of parameters: per tensor, its fp32 master weights (updated
  * in place), an optional bf16 copy (master_bf16 NULL or master_bf16[i]
  * NULL: none) and its fp32 gradients (typically the outs of a
- * gs_tensor_list).  Allocates a device chunk table (synchronous). */
+ * gs_tensor_list).  Allocates a device chunk table and returns once it is
+ * on the device (it synchronises the legacy default stream). */
 typedef struct gs_param_list gs_param_list;
 int gs_param_list_create(float* const* master, uint16_t* const* master_bf16,
                          const float* const* grads, const int64_t* numels, int32_t n_tensors,

@@ -290,14 +290,18 @@ int gs_tensor_list_create(const void* const* grads, void* const* outs, const int
   if (!l) return GS_ERR_ARG;
   const size_t ws_bytes = 256 + (size_t)sm_count() * kUnscaleCtasPerSm * sizeof(double);
   cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&l->d_ws), ws_bytes);
-  if (e == cudaSuccess) e = cudaMemset(l->d_ws, 0, ws_bytes);
+  if (e == cudaSuccess) e = cudaMemsetAsync(l->d_ws, 0, ws_bytes, cudaStreamLegacy);
   l->d_norm_slots = reinterpret_cast<double*>(reinterpret_cast<char*>(l->d_ws) + 256);
   if (e == cudaSuccess && !chunks.empty()) {
     e = cudaMalloc(reinterpret_cast<void**>(&l->d_chunks), chunks.size() * sizeof(Chunk));
     if (e == cudaSuccess)
-      e = cudaMemcpy(l->d_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
-                     cudaMemcpyHostToDevice);
+      e = cudaMemcpyAsync(l->d_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
+                          cudaMemcpyHostToDevice, cudaStreamLegacy);
   }
+  // Both must have landed before the call returns: a step launched next on a
+  // non-blocking stream is not ordered behind the legacy stream, and a copy
+  // from pageable memory may return before its data reaches the device.
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamLegacy);
   if (e != cudaSuccess) {
     if (l->d_chunks) cudaFree(l->d_chunks);
     if (l->d_ws) cudaFree(l->d_ws);
@@ -420,8 +424,10 @@ int gs_param_list_create(float* const* master, uint16_t* const* master_bf16,
   if (!chunks.empty()) {
     e = cudaMalloc(reinterpret_cast<void**>(&l->d_chunks), chunks.size() * sizeof(MChunk));
     if (e == cudaSuccess)
-      e = cudaMemcpy(l->d_chunks, chunks.data(), chunks.size() * sizeof(MChunk),
-                     cudaMemcpyHostToDevice);
+      e = cudaMemcpyAsync(l->d_chunks, chunks.data(), chunks.size() * sizeof(MChunk),
+                          cudaMemcpyHostToDevice, cudaStreamLegacy);
+    // landed before the call returns (as for gradient lists)
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamLegacy);
   }
   if (e != cudaSuccess) {
     if (l->d_chunks) cudaFree(l->d_chunks);

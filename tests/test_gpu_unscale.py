@@ -416,3 +416,26 @@ def test_scaler_state_in_host_memory(gs, orc):
     assert ei.value.status == gs.GS_ERR_ARG
     assert float(pageable[0][0]) == 1024.0 and int(pageable[1][0]) == 0
     tl.close()
+
+
+def test_list_is_ready_for_a_step_on_another_stream(gs):
+    """gs_tensor_list_create returns once its chunk table and workspace are
+    on the device, so a step launched right after it on a non-blocking
+    stream (not ordered behind the stream the table was uploaded on) reads
+    the whole table: a 1000-tensor list, ten times over, each step checked."""
+    rng = np.random.default_rng(11)
+    sizes = rng.integers(1, 20000, 1000).tolist()
+    grads = [torch.from_numpy((rng.standard_normal(n) * 50).astype(np.float16)).to(DEV) for n in sizes]
+    want = [g.float() / 1024.0 for g in grads]
+    side = torch.cuda.Stream()
+    for _ in range(10):
+        outs = [torch.empty(n, dtype=torch.float32, device=DEV) for n in sizes]
+        state = _state(1024.0)
+        torch.cuda.synchronize()
+        tl = gs.gs_tensor_list_create(grads, outs)
+        with torch.cuda.stream(side):
+            gs.gs_unscale_check_update(tl, *state, 2.0, 0.5, 2000)
+        side.synchronize()
+        assert int(state[2].item()) == 0
+        assert all(torch.equal(o, w) for o, w in zip(outs, want))
+        tl.close()
