@@ -82,9 +82,12 @@ const char* gs_version(void);
 
 /* Opaque description of one gradient list: for each tensor, its scaled
  * FP16 gradient (input), its FP32 unscaled output and its element count.
- * The handle owns a device-resident table that cuts the list into
- * equal-sized chunks, built once so that each step walks the whole list in
- * a single grid, plus a 16-byte device workspace. */
+ * The handle owns a device-resident table that cuts each tensor into chunks
+ * of 8192 elements (after a short head chunk up to its first element where
+ * input and output are both 32-byte aligned), built once so that each step
+ * walks the whole list in a single grid, plus a device workspace: 256 bytes
+ * for the step's epilogue words and one fp64 slot per CTA of the unscale
+ * grid for the norm form. */
 typedef struct gs_tensor_list gs_tensor_list;
 
 /* Build a list on the current device.
