@@ -5,8 +5,9 @@ and the benchmark's CPU-baseline leg may import this package.  The product
 library never loads it, and it never loads the product library.
 
 The arithmetic lives in plain C (``fp_formats.c``, ``gradscaler.c``,
-``fp8_quant.c``), compiled with ``gcc -O2 -ffp-contract=off``.  This module
-only builds that library and marshals numpy arrays into it.
+``fp8_quant.c``, ``mx_quant.c``, ``delayed.c``, ``master.c``, ``gemm.c``),
+compiled with ``gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math``.  This
+module only builds that library and marshals numpy arrays into it.
 """
 from __future__ import annotations
 
