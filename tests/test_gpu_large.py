@@ -1,5 +1,6 @@
 """The 128x128, per-tensor, MXFP8 and delayed-scaling quantisers on single
-tensors past 2^32 elements (8 GiB of bf16 input), against the oracle ("Mixed
+tensors past 2^32 elements (8 GiB of bf16 input), and the block-scaled GEMM
+writing an output past 2^31 elements, against the oracle ("Mixed
 precision and FP8 training", section "FP8 training": per_block, per_tensor,
 and the MX formats' one scale per 32 elements; "Why FP8 training is stable",
 "Failure 1": one scale for the whole tensor, or one from a history).  Element
@@ -177,3 +178,41 @@ def test_quant_delayed_past_2_32_elements(gs, orc):
     assert_same_bytes(got, want, "delayed codes at sampled positions")
     del q
     torch.cuda.empty_cache()
+
+
+def test_gemm_output_past_2_31_elements(gs, orc):
+    """The block-scaled FP8 GEMM with D = [65537, 32776] fp32 (2.15e9
+    elements, 8.6 GB; ragged in M and N), once with D 16-byte aligned (TMA
+    stores) and once at a 4-byte offset (element stores): exact-value inputs
+    (codes of -2..2, power-of-two scales, so every element is exact in fp32),
+    compared bit for bit with the oracle at the corners, around linear
+    element 2^31 and at 10^4 seeded positions ("Mixed precision and FP8
+    training", section "FP8 training": promotion every 128 elements)."""
+    M, N, K = 65537, 32776, 256
+    rng = np.random.default_rng(31)
+    table = orc.fp8_decode_array(np.arange(256, dtype=np.uint8), orc.E4M3)
+    lut = np.array([int(np.flatnonzero(table == v)[0]) if v else 0
+                    for v in (-2.0, -1.0, 0.0, 1.0, 2.0)], np.uint8)
+    qa_h = lut[rng.integers(0, 5, (M, K))]
+    qb_h = lut[rng.integers(0, 5, (N, K))]
+    sa_h = np.exp2(rng.integers(-2, 3, (M, K // 128))).astype(np.float32)
+    sb_h = np.exp2(rng.integers(-2, 3, ((N + 127) // 128, K // 128))).astype(np.float32)
+    qa, qb = torch.from_numpy(qa_h).to(DEV), torch.from_numpy(qb_h).to(DEV)
+    sa, sb = torch.from_numpy(sa_h).to(DEV), torch.from_numpy(sb_h).to(DEV)
+    lin = [0, N - 1, (M - 1) * N, M * N - 1] + [(1 << 31) + d for d in range(-3, 4)]
+    lin += rng.integers(0, M * N, 10000).tolist()
+    lin = np.array(lin, np.int64)
+    want = np.array([orc.gemm_fp8_block_elem(qa_h, sa_h, qb_h, sb_h, int(i // N), int(i % N),
+                                             orc.E4M3) for i in lin]).astype(np.float32)
+    idx = torch.from_numpy(lin).to(DEV)
+    for off in (0, 1):  # in fp32 elements: 0 takes the TMA stores, 1 the element stores
+        buf = torch.full((M * N + off,), float("nan"), dtype=torch.float32, device=DEV)
+        d = buf[off:].view(M, N)
+        gs.fp8_gemm_block_scaled(qa, sa, qb, sb, "e4m3", d)
+        got = d.view(-1)[idx].cpu().numpy()
+        del d, buf
+        torch.cuda.empty_cache()
+        bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
+        assert bad.size == 0, (f"offset {off}: {bad.size} elements differ, first at linear "
+                               f"{lin[bad[0]]}: {got[bad[0]]} != {want[bad[0]]}")
+    assert gs.gs_device_status() == gs.GS_OK
