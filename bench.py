@@ -100,6 +100,44 @@ def aggregate(elapsed_s: float, units: float, dist=None, device=None) -> tuple[f
     return float(t.item()), float(u.item())
 
 
+def host_memory_available(meminfo: str = None, cgroup: tuple = None):
+    """Bytes of host memory still available to this process: MemAvailable
+    from /proc/meminfo, capped by what the cgroup's memory limit leaves (v2
+    or v1). None when neither can be read."""
+    avail = None
+    try:
+        if meminfo is None:
+            with open("/proc/meminfo") as f:
+                meminfo = f.read()
+        for line in meminfo.splitlines():
+            if line.startswith("MemAvailable:"):
+                avail = int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    pairs = [cgroup] if cgroup else [("/sys/fs/cgroup/memory.max", "/sys/fs/cgroup/memory.current"),
+                                     ("/sys/fs/cgroup/memory/memory.limit_in_bytes",
+                                      "/sys/fs/cgroup/memory/memory.usage_in_bytes")]
+    for lim_f, cur_f in pairs:
+        try:
+            with open(lim_f) as f:
+                lim = f.read().strip()
+            with open(cur_f) as f:
+                cur = int(f.read().strip())
+        except (OSError, ValueError):
+            continue
+        if lim != "max" and int(lim) < (1 << 60):
+            room = max(int(lim) - cur, 0)
+            avail = room if avail is None else min(avail, room)
+        break
+    return avail
+
+
+def e2e_fits(pinned_bytes: int, local_ranks: int, available) -> bool:
+    """True when the pinned host buffers of every rank on this node take at
+    most 60% of the host memory available (or when it cannot be read)."""
+    return available is None or pinned_bytes * local_ranks <= 0.6 * available
+
+
 def throughput(total_bytes: float, elapsed_s: float) -> float:
     return total_bytes / elapsed_s / 1e9
 
@@ -354,6 +392,14 @@ class Workload:
     # overwritten while a copy or a kernel still uses it.  Each gradient list
     # and its outputs live in one flat buffer, so a step is 4 copies up and
     # 11 down.
+    def e2e_host_bytes(self) -> int:
+        """Pinned host bytes e2e_setup allocates: the step's inputs and all its
+        results (and the scaler state), one copy each."""
+        ins = [self.g_flat, self.x3, self.x4, self.x5]
+        res = [self.o_flat, self.q3, self.s3, self.y3, self.q4, self.s4, self.q5, self.s5,
+               self.scale, self.tracker, self.found]
+        return sum(t.numel() * t.element_size() for t in ins + res)
+
     def e2e_setup(self):
         torch, gs = self.torch, self.gs
         pin = dict(pin_memory=True)
@@ -654,6 +700,21 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
+        # every rank pins its own copy of the step's inputs and results: run
+        # e2e only if all of this node's ranks fit in the host's memory (the
+        # decision is the same on every rank, or the collectives below hang)
+        need = w.e2e_host_bytes()
+        local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+        avail = host_memory_available()
+        ok = torch.tensor([1 if e2e_fits(need, local_ranks, avail) else 0], device=dev)
+        if dist:
+            dist.all_reduce(ok, op=dist.ReduceOp.MIN)
+        if not int(ok.item()):
+            e2e = {"value": None, "unit": UNIT,
+                   "skipped": f"pinned host buffers of {need / 1e9:.1f} GB per rank x "
+                              f"{local_ranks} ranks exceed 60% of the host memory available "
+                              f"({(avail or 0) / 1e9:.0f} GB) on some node"}
+    if not args.no_e2e and e2e is None:
         w.e2e_setup()
         for k in range(2):
             w.e2e_step(k)

@@ -116,3 +116,23 @@ def test_link_ceiling_two_phase():
     assert bench.link_ceiling(30e9, 20e9, 10e9, 25.0, 400.0, 100.0) == pytest.approx(50.0)
     # equal transfers never leave the shared phase
     assert bench.link_ceiling(2e9, 1e9, 1e9, 999.0, 999.0, 100.0) == pytest.approx(100.0)
+
+
+def test_host_memory_available_and_the_e2e_check(tmp_path):
+    """MemAvailable, capped by what a cgroup limit leaves; e2e runs only when
+    every local rank's pinned buffers fit in 60% of it."""
+    import bench
+    meminfo = "MemTotal:       500000000 kB\nMemAvailable:   400000000 kB\n"
+    lim, cur = tmp_path / "memory.max", tmp_path / "memory.current"
+    lim.write_text("max\n")
+    cur.write_text("123\n")
+    assert bench.host_memory_available(meminfo, (str(lim), str(cur))) == 400000000 * 1024
+    lim.write_text(str(100 * 2 ** 30) + "\n")
+    cur.write_text(str(40 * 2 ** 30) + "\n")
+    assert bench.host_memory_available(meminfo, (str(lim), str(cur))) == 60 * 2 ** 30
+    assert bench.host_memory_available("", (str(tmp_path / "none"), str(cur))) is None
+    assert isinstance(bench.host_memory_available(), (int, type(None)))
+    step = 50.3e9  # the benchmark step's pinned inputs and results
+    assert bench.e2e_fits(step, 1, 400e9)
+    assert not bench.e2e_fits(step, 8, 400e9)
+    assert bench.e2e_fits(step, 8, None)
