@@ -43,6 +43,12 @@ def _bf16(rng, shape):
     return torch.from_numpy((rng.standard_normal(shape) * 3).astype(np.float32)).to(DEV).to(torch.bfloat16)
 
 
+def _input(rng, shape, dt):
+    """bf16 or fp32 input (fp32 takes the quantisers' fp32 kernels)."""
+    x = _bf16(rng, shape)
+    return x if dt == "bf16" else x.float()
+
+
 @pytest.mark.parametrize("off", [0, 4, 16, 36])
 def test_unscale_outputs_keep_their_guards(gs, off):
     rng = np.random.default_rng(off)
@@ -62,12 +68,13 @@ def test_unscale_outputs_keep_their_guards(gs, off):
     assert all(torch.equal(o.t, r) for o, r in zip(outs, ref))
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("br", [1, 128])
 @pytest.mark.parametrize("q_off", [0, 8, 1])
-def test_quant_block_codes_and_scales_keep_their_guards(gs, br, q_off):
+def test_quant_block_codes_and_scales_keep_their_guards(gs, br, q_off, dt):
     rng = np.random.default_rng(br + q_off)
     R, C = (384, 640) if br == 128 else (7, 1152)
-    x = _bf16(rng, (R, C))
+    x = _input(rng, (R, C), dt)
     q = Guarded(R * C, torch.uint8, (R, C), q_off)
     s = Guarded(4 * (R // br) * (C // 128), torch.float32, (R // br, C // 128), 4 * (q_off % 2))
     gs.fp8_quant_block(x, br, 128, "e4m3", q.t, s.t)
@@ -82,10 +89,11 @@ def test_quant_block_codes_and_scales_keep_their_guards(gs, br, q_off):
         assert y.intact(), f"dequant {out} wrote outside its output"
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("n,q_off", [(1, 0), (1000003, 0), (1000003, 3), (4096 * 33, 8)])
-def test_quant_tensor_and_delayed_keep_their_guards(gs, n, q_off):
+def test_quant_tensor_and_delayed_keep_their_guards(gs, n, q_off, dt):
     rng = np.random.default_rng(n + q_off)
-    x = _bf16(rng, (n,))
+    x = _input(rng, (n,), dt)
     ws = torch.empty(gs.gs_ws_bytes() // 4, dtype=torch.int32, device=DEV)
     q = Guarded(n, torch.uint8, (n,), q_off)
     s = Guarded(4, torch.float32, (1,))
@@ -102,11 +110,12 @@ def test_quant_tensor_and_delayed_keep_their_guards(gs, n, q_off):
     assert q2.intact() and hist.intact() and used.intact()
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("q_off", [0, 1])
-def test_mx_codes_scales_and_dequant_keep_their_guards(gs, q_off):
+def test_mx_codes_scales_and_dequant_keep_their_guards(gs, q_off, dt):
     rng = np.random.default_rng(q_off)
     R, C = 5, 96
-    x = _bf16(rng, (R, C))
+    x = _input(rng, (R, C), dt)
     q = Guarded(R * C, torch.uint8, (R, C), q_off)
     s = Guarded(R * C // 32, torch.uint8, (R, C // 32), q_off)
     gs.fp8_quant_mx(x, "e4m3", q.t, s.t)
