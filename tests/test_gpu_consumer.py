@@ -7,7 +7,7 @@ import torch
 import datagen as dg
 from datagen import workloads as wl
 from conftest import load_golden
-from gpu_helpers import DEV, assert_same_f32, bits_of, same_bf16, to_dev16
+from gpu_helpers import DEV, assert_same_f32, bits_of, pmap, same_bf16, to_dev16
 
 pytestmark = pytest.mark.gpu
 
@@ -235,4 +235,55 @@ def test_norm_one_llama_layer(gs, orc):
     torch.cuda.synchronize()
     assert s[2].item() == ref_found == 0
     assert abs(norm.item() ** 2 - want ** 2) <= NORM_REL_TOL * want ** 2, (norm.item(), want)
+    tl.close()
+
+
+def test_norm_and_master_update_two_llama_layers(gs, orc):
+    """The norm form and the master update at the size the benchmark times
+    them (the first two layers of the Llama-3-8B list: 18 tensors, 436 M
+    elements, the same launches): the norm against the oracle's compensated
+    sum over every host-regenerated unscaled gradient; then SGD without
+    clipping on fp32 masters (bf16 N(0, 0.02) values widened exactly) with
+    a bf16 copy, bit for bit against the oracle at 2^14 seeded positions of
+    every tensor, whose gradients and masters are regenerated on the host."""
+    cfg = wl.cfg2_grads()
+    sizes = cfg.numels[:18]
+    st = torch.cuda.current_stream().cuda_stream
+    grads = [torch.empty(n, dtype=torch.float16, device=DEV) for n in sizes]
+    for t, g in enumerate(grads):
+        dg.fill_device(cfg.spec(t, 0), 0, g.numel(), g.data_ptr(), st)
+    outs = [torch.empty(n, dtype=torch.float32, device=DEV) for n in sizes]
+    tl = gs.gs_tensor_list_create(grads, outs)
+    s = _state()
+    norm = torch.empty(1, dtype=torch.float32, device=DEV)
+    gs.gs_unscale_check_update_norm(tl, *s, norm, None, 2.0, 0.5, 2000)
+    wspec = [dg.normal_bf16(wl.seed_of(2) + 7, t, 0.02, n) for t, n in enumerate(sizes)]
+    w = []
+    for sp, n in zip(wspec, sizes):
+        b = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+        dg.fill_device(sp, 0, n, b.data_ptr(), st)
+        w.append(b.float())
+    wb = [torch.zeros(n, dtype=torch.bfloat16, device=DEV) for n in sizes]
+    pl = gs.gs_param_list_create(w, outs, wb)
+    lr = 1e-4
+    gs.gs_master_update_sgd(pl, lr, 0.0, None, s[2])
+
+    def sum_sq(t):
+        out, _ = orc.unscale_check(dg.fill_host(cfg.spec(t, 0), 0, sizes[t]), 2.0 ** 16)
+        return orc.grad_norm([out]) ** 2
+
+    want = float(np.sqrt(sum(pmap(sum_sq, range(len(sizes))))))
+    torch.cuda.synchronize()
+    assert s[2].item() == 0
+    assert abs(norm.item() ** 2 - want ** 2) <= NORM_REL_TOL * want ** 2, (norm.item(), want)
+    rng = np.random.default_rng(436)
+    for t, n in enumerate(sizes):
+        idx = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 1 << 14)]))
+        g_ref, _ = orc.unscale_check(dg.fill_host_idx(cfg.spec(t, 0), idx), 2.0 ** 16)
+        ref_w = (dg.fill_host_idx(wspec[t], idx).astype(np.uint32) << 16).view(np.float32)
+        ref_b = orc.master_update_sgd(ref_w, g_ref, lr, 1.0, 0)
+        it = torch.from_numpy(idx).to(DEV)
+        assert_same_f32(w[t][it].cpu().numpy(), ref_w, f"tensor {t} masters")
+        assert same_bf16(bits_of(wb[t][it]), ref_b).all(), f"tensor {t} bf16 copy"
+    pl.close()
     tl.close()
