@@ -262,14 +262,19 @@ def test_cfg3_full_size_sampled(gs, orc):
     assert float(s.max()) > 100 / 448
 
 
-def test_cfg4_weight_128x128_full_size(gs, orc):
+@pytest.mark.parametrize("x_off", [0, 8])
+def test_cfg4_weight_128x128_full_size(gs, orc, x_off):
     """Config 4 weights: bf16 8192x28672 N(0,0.02), 14 hot blocks x100, E4M3
-    128x128 (32-byte aligned input: the direct-load kernel).  The oracle
-    quantises the host-regenerated weight, one 128-row block-row per host
-    thread: every one of the 235e6 codes and 14336 scales is compared."""
+    128x128, as the benchmark runs them: 32-byte aligned input (the 32-byte
+    load kernel) and input at a 16-byte offset (the 16-byte load kernel).
+    The oracle quantises the host-regenerated weight, one 128-row block-row
+    per host thread: every one of the 235e6 codes and 14336 scales is
+    compared."""
     w = wl.cfg4_weight()
     st = torch.cuda.current_stream().cuda_stream
-    x = torch.empty(w.rows, w.cols, dtype=torch.bfloat16, device=DEV)
+    xbuf = torch.empty(w.numel + x_off, dtype=torch.bfloat16, device=DEV)
+    x = xbuf[x_off:].view(w.rows, w.cols)
+    assert x.data_ptr() % 32 == 2 * x_off
     dg.fill_device(w.spec, 0, w.numel, x.data_ptr(), st)
     q = torch.empty(w.rows, w.cols, dtype=torch.uint8, device=DEV)
     s = torch.empty(w.rows // 128, w.cols // 128, dtype=torch.float32, device=DEV)
