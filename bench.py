@@ -65,7 +65,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--sweep", action="store_true", help="bandwidth sweep 1 MiB..8 GiB (config 5)")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--only", choices=ONLY_CASES,
                    help="time one kernel alone on a small case (for ncu captures)")
